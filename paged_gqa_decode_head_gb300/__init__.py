@@ -1,0 +1,22 @@
+"""Paged GQA decode attention for GB300 (sm_103a).
+
+The compute path is the C-ABI library ``libpgqa.so`` built from ``csrc/``;
+``binding`` marshals arguments to it through ctypes. Importing this package
+does not load the library: the first call of a binding function does, and it
+raises if the library is missing (there is no CPU fallback).
+"""
+from .binding import (  # noqa: F401
+    PgqaError,
+    attn_host_tiled_run,
+    attn_partition_merge,
+    attn_tile_finalize,
+    attn_tile_init,
+    attn_tile_update,
+    decode_attn_paged,
+    decode_attn_partition_count,
+    decode_attn_workspace_size,
+    device_error_flags,
+    library_path,
+    load_library,
+    qk_norm_rope_append,
+)

@@ -1,0 +1,387 @@
+"""Benchmark of the paged GQA decode step on GB300.
+
+Workload (default): Qwen3-0.6B-shaped decode -- 28 layers, each with its own
+paged bf16 KV cache of T = 8192 positions (Hkv = 8, D = 128, page size 16,
+random block table; 896 MiB of KV in total), B = 1, Hq = 16. One step runs,
+for every layer, the fused prologue (Q/K RMSNorm, RoPE, K/V append) and the
+split-KV paged decode attention with its partition merge, all captured in one
+CUDA graph. Each layer's 32 MiB is read once per step and 27 other layers
+are read in between, so the working set (896 MiB) is far larger than L2.
+
+Metric: decode-attention KV GB/s (K+V bytes the attention must read, divided
+by the step time) and microseconds per layer-step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, plain C) on the host cores on a
+bounded sample of the same workload. Under torchrun every rank runs an
+independent replica (the step does not shard across GPUs) and rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention KV GB/s (fraction of HBM peak); µs per layer-step at T=8K"
+WORKLOAD = "qwen3_0p6b_t8k"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_kernel_qwen3_t8k.md")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_gqa_decode_head_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    only if it was taken on the current kernel sources."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not traffic or sha.group(1) != kernel_source_sha():
+        return None
+    return float(traffic.group(1))
+
+
+def smi_gpu_id(dev) -> str:
+    """nvidia-smi identifier (UUID when torch exposes it) of a torch device."""
+    import torch
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = dev.index or 0
+        if vis:
+            return vis.split(",")[idx].strip()
+        return str(idx)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples in the background (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        window = [p for (t, p) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not window:
+            window = [p for (_, p) in self.samples]
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in window if num(p[1]) is not None]
+        smax = [num(p[2]) for p in window if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in window:
+            for name, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(window)}
+
+
+# ------------------------------------------------------------------ oracle (CPU) leg
+def oracle_layer(layer, theta):
+    import oracle
+
+    kv, tok = layer
+    q_ref, kc, vc = oracle.qk_norm_rope_append(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k, kv.context_lens,
+                                               kv.block_table, kv.k_cache, kv.v_cache, kv.page_size, theta)
+    oracle.decode_attention(q_ref, kc, vc, kv.block_table, kv.context_lens, 1.0 / math.sqrt(128))
+
+
+def time_oracle(layers, theta, n_layer_evals: int):
+    """Run the oracle's prologue + attention on n_layer_evals layers (cycling
+    through the step's layers) on all host cores; returns (seconds, cores)."""
+    import oracle
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    jobs = [layers[i % len(layers)] for i in range(n_layer_evals)]
+    t0 = time.perf_counter()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:  # ctypes releases the GIL
+        list(ex.map(lambda lay: oracle_layer(lay, theta), jobs))
+    return time.perf_counter() - t0, min(cores, n_layer_evals)
+
+
+def kv_bytes_layer(T, Hkv=8, D=128):
+    return 4 * T * Hkv * D
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from paged_gqa_decode_head_gb300 import inputs
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    n_layers = args.layers or w["layers"]
+    layers = inputs.qwen3_layers(layers=n_layers)
+    sample_layers = min(n_layers, 8)  # one step of the reference arm = 8 of the 28 layers
+    for _ in range(args.warmup):
+        time_oracle(layers, w["theta"], sample_layers)
+    total_s = 0.0
+    cores = 1
+    for _ in range(args.steps):
+        s, cores = time_oracle(layers, w["theta"], sample_layers)
+        total_s += s
+    layer_s = total_s / (args.steps * sample_layers)
+    gbs = kv_bytes_layer(w["T"]) / layer_s / 1e9
+    sample = (f"{sample_layers} of the {n_layers} layers per step (prologue + full-softmax attention, T={w['T']}), "
+              f"fp64 oracle, layers spread over {cores} host threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "us_per_layer_step": layer_s * 1e6,
+        "config": {"workload": WORKLOAD, "layers": n_layers, "B": 1, "Hq": 16, "Hkv": 8, "D": 128, "T": w["T"],
+                   "page_size": 16},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+def run_ours(args, rank, world, local):
+    import torch
+
+    import paged_gqa_decode_head_gb300 as pg
+    from paged_gqa_decode_head_gb300 import inputs
+    from paged_gqa_decode_head_gb300.runner import DecodeStep
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    pg.load_library()
+    w = inputs.WORKLOADS[WORKLOAD]
+    n_layers = args.layers or w["layers"]
+    layers = inputs.qwen3_layers(layers=n_layers)
+
+    # CPU-baseline leg first (rank 0, one GPU job only), before any GPU work
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample_layers = n_layers
+        s, cores = time_oracle(layers, w["theta"], sample_layers)
+        gbs = kv_bytes_layer(w["T"]) * sample_layers / s / 1e9
+        cpu_baseline = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                        "sample": f"one full step ({sample_layers} layers, prologue + full-softmax attention, "
+                                  f"T={w['T']}) of the fp64 oracle, layers spread over {cores} host threads"}
+
+    step = DecodeStep(layers, Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"], device=dev)
+    np_used = step.partitions
+    attn_graph = step.capture(prologue=False)  # attention only, same buffers
+    step_graph = step.capture(prologue=True)  # the whole step
+    stream = torch.cuda.current_stream(dev)
+
+    kv_bytes = sum(kv_bytes_layer(int(kv.context_lens.sum())) for kv, _ in layers)
+    algo_bytes_layer = (kv_bytes_layer(w["T"]) + 2 * w["Hq"] * 128 + 4 * math.ceil(w["T"] / 16)
+                        + 6 * w["Hq"] * 128)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(fn, steps):
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for _ in range(max(3, args.warmup)):
+        step_graph.replay()
+    for _ in range(max(3, args.warmup)):
+        attn_graph.replay()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(smi_gpu_id(dev))
+    sampler.start()
+    time.sleep(0.5)
+    t_wall0 = time.time()
+    ms = timed(step_graph.replay, args.steps)
+    t_wall1 = time.time()
+    ms_attn = timed(attn_graph.replay, args.steps)
+    t_wall2 = time.time()
+
+    # end to end through the public API: per step the new tokens (q, k, v of
+    # every layer) come from pinned host memory and the outputs go back.
+    host_in = []
+    for kv, tok in layers:
+        host_in.append([torch.from_numpy(a.view("int16")).view(torch.bfloat16).pin_memory()
+                        for a in (tok.q, tok.k, tok.v)])
+    host_out = [torch.empty(st.out_f32.shape, dtype=torch.float32).pin_memory() for st in step.layers]
+    h2d = sum(t.numel() * 2 for trio in host_in for t in trio)
+    d2h = sum(t.numel() * 4 for t in host_out)
+
+    def e2e_step():
+        for trio, st in zip(host_in, step.layers):
+            st.q.copy_(trio[0], non_blocking=True)
+            st.k.copy_(trio[1], non_blocking=True)
+            st.v.copy_(trio[2], non_blocking=True)
+        step_graph.replay()
+        for ho, st in zip(host_out, step.layers):
+            ho.copy_(st.out_f32, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(1, min(args.steps, 500))
+    ms_e2e = timed(e2e_step, e2e_steps)
+    t_wall3 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall3)
+    assert pg.device_error_flags() == 0, "device error flags raised during the benchmark"
+
+    step_s = ms / args.steps / 1e3
+    value = world * kv_bytes / step_s / 1e9
+    layer_attn_s = ms_attn / args.steps / 1e3 / n_layers
+    achieved = algo_bytes_layer / layer_attn_s / 1e9
+    peak, peak_kind = load_peaks()
+    e2e_s = ms_e2e / e2e_steps / 1e3
+    launches_per_layer = 2 + (1 if np_used > 1 else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "us_per_layer_step": step_s * 1e6 / n_layers,
+        "attention_us_per_layer": layer_attn_s * 1e6,
+        "hbm_fraction_of_step": value / world / peak,
+        "config": {"workload": WORKLOAD, "layers": n_layers, "B": 1, "Hq": w["Hq"], "Hkv": w["Hkv"], "D": 128,
+                   "T": w["T"], "page_size": 16, "num_partitions": np_used, "graph": "one CUDA graph per step",
+                   "l2": "inputs larger than L2: 896 MiB of KV, each layer's 32 MiB read once per step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                     "kernel": "decode_split_kernel (+ merge), timed as an attention-only graph of "
+                               f"{n_layers} layers, CUDA events on the launch stream"},
+        "e2e": {"value": world * kv_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": args.steps * n_layers * launches_per_layer,
+        "clocks": clocks,
+        "cpu_baseline": cpu_baseline,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.gpus != world and world != 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

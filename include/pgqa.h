@@ -1,0 +1,216 @@
+/*
+ * pgqa.h -- C ABI of the paged GQA decode-attention library (libpgqa.so),
+ * sm_103a (GB300).
+ *
+ * The library computes the single-token decode step of grouped-query
+ * attention over a paged bf16 KV cache:
+ *   - the fused prologue: per-head Q/K RMSNorm, half-rotation RoPE and the
+ *     append of the new token's K/V into the paged cache;
+ *   - decode attention with (m, l, acc) online softmax, split over KV
+ *     partitions and merged exactly;
+ *   - a host-tiled variant that keeps (m, l, acc) in global memory while KV
+ *     tiles are streamed in from pinned host memory.
+ *
+ * Sources (page title, section):
+ *   "From Qwen3 math to CUDA kernels: a 0.6B inference runtime"
+ *       s2.1 RMSNorm, s2.3 Q/K head RMSNorm, s2.4 RoPE, s2.5 GQA head map,
+ *       s2.6 scaled dot-product attention (causal), s5.1 current stream,
+ *       s5.2 no allocation on the hot path, s7.1 one warp per head,
+ *       s7.2 logical token -> physical cache address, s9.1 exact partition
+ *       merge, s10.1 grouped single-CTA path, s10.2 partitioned path.
+ *   "EdgeTransformerEngine"
+ *       online-softmax note (state (m, l, acc) and its update step),
+ *       KV-offload design (attn_init / attn_tile / attn_finalize kernels,
+ *       512-position tiles, m = -1e30), copy/compute stream events.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Types. pgqa_bf16 is a bf16 bit pattern (the top half of a binary32).
+ *   All float state is IEEE binary32. Index arrays are int32.
+ * Shapes. D (head dimension) must be 128. Hq % Hkv == 0 and the group size
+ *   g = Hq / Hkv must lie in [1, 8]. Query head h reads KV head h / g.
+ * Cache layout. k_cache and v_cache are [num_pages][Hkv][page_size][D] bf16:
+ *   the rows of one (physical page, KV head) are contiguous. Position pos of
+ *   sequence b lives in physical page block_table[b * max_pages + pos /
+ *   page_size] at in-page offset pos % page_size. page_size is a power of two
+ *   in [16, 256].
+ * Context lengths. context_lens[b] = T_b counts the new token, which sits at
+ *   position T_b - 1 and attends to all T_b positions (itself included).
+ * Memory. Every pointer is caller-owned device memory unless stated
+ *   otherwise; the library never allocates or frees memory. Tensor pointers
+ *   (bf16 and float arrays) must be 16-byte aligned; index arrays 4-byte.
+ * Streams. All work is enqueued on the stream the caller passes; nothing is
+ *   synchronised and the default stream is never used implicitly. Calls are
+ *   capturable into CUDA graphs except pgqa_device_error (synchronous).
+ * Errors. Every call returns PGQA_OK (0) or a negative PGQA_ERR_* code and
+ *   never throws; pgqa_last_error() returns the calling thread's message for
+ *   its last failing call. Invalid data that only the device can see (a
+ *   block-table entry outside [0, num_pages), a context length above
+ *   max_pages * page_size) never causes an out-of-bounds access: the
+ *   affected keys or slots are skipped and a sticky per-device flag is
+ *   raised, readable with pgqa_device_error().
+ */
+#ifndef PGQA_H
+#define PGQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pgqa_bf16;
+
+enum pgqa_status {
+    PGQA_OK = 0,
+    PGQA_ERR_INVALID_ARG = -1, /* null pointer, negative size, inconsistent shapes */
+    PGQA_ERR_UNSUPPORTED = -2, /* D != 128, g outside [1, 8], page_size not in {16..256} */
+    PGQA_ERR_MISALIGNED = -3,  /* a tensor pointer is not 16-byte aligned */
+    PGQA_ERR_WORKSPACE = -4,   /* workspace missing or smaller than required */
+    PGQA_ERR_CUDA = -5         /* a CUDA runtime call or launch failed */
+};
+
+/* Sticky device-side flags (bit mask) read by pgqa_device_error(). */
+#define PGQA_DEVERR_BAD_PAGE 1u     /* block-table entry outside [0, num_pages) */
+#define PGQA_DEVERR_BAD_CONTEXT 2u  /* context length < 0 (or < 1 for the prologue) or too long */
+#define PGQA_DEVERR_WAIT_TIMEOUT 4u /* an asynchronous copy did not complete in time */
+
+/* Message of the calling thread's last failing call ("" if none). */
+const char *pgqa_last_error(void);
+
+/* Read the sticky device flags of the current device into *flags_out (OR of
+ * PGQA_DEVERR_*) and clear them if clear != 0. Synchronises the device. */
+int pgqa_device_error(unsigned *flags_out, int clear);
+
+/*
+ * qk_norm_rope_append -- fused decode prologue for one layer.
+ * Follows s2.3 (per-head RMSNorm with learned gains, eps), s2.4 (RoPE on the
+ * pairs (i, i + D/2), omega_i = theta^(-2i/D), phase pos * omega_i), s7.1
+ * (one warp per head) and s7.2 (write the rotated K straight into its
+ * physical page).
+ *
+ *   q       [B][Hq][D]  bf16   new token's query heads
+ *   k, v    [B][Hkv][D] bf16   new token's key / value heads
+ *   gamma_q, gamma_k [D] bf16  RMSNorm gains (shared by all heads)
+ *   context_lens [B] int32     T_b >= 1; the new token sits at pos = T_b - 1
+ *   block_table [B][max_pages] int32
+ *   k_cache, v_cache           paged cache (layout above); only the slots
+ *                              (b, h, pos) are written: K = bf16(RoPE(RMSNorm(k))),
+ *                              V = v bit for bit
+ *   q_out   [B][Hq][D]  bf16   bf16(RoPE(RMSNorm(q)))
+ * Arithmetic in fp32; the RoPE phase is formed and reduced in fp64 so that it
+ * stays accurate at large positions. bf16 results are rounded to nearest even.
+ * A sequence with an invalid T_b or page is skipped (flag raised).
+ */
+int qk_norm_rope_append(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                        const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                        const int32_t *context_lens, const int32_t *block_table,
+                        pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq,
+                        int Hkv, int D, int page_size, int max_pages, int num_pages,
+                        float rope_theta, float eps, cudaStream_t stream);
+
+/*
+ * decode_attn_partition_count -- number of KV partitions NP that
+ * decode_attn_paged will use for these arguments (num_partitions = 0 picks
+ * one from the current device's SM count; otherwise it is clamped to
+ * [1, max_pages]). Each partition covers ceil(max_pages / NP) pages.
+ */
+int decode_attn_partition_count(int B, int Hkv, int page_size, int max_pages,
+                                int num_partitions);
+
+/*
+ * decode_attn_workspace_size -- bytes of device workspace decode_attn_paged
+ * needs (0 when NP = 1). Same arguments as decode_attn_paged; the auto
+ * choice depends on the current device.
+ */
+size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                  int num_partitions);
+
+/*
+ * decode_attn_paged -- causal GQA decode attention over the paged cache.
+ * Follows s2.5/s2.6 (query head h attends with KV head h/g over positions
+ * 0 .. T_b - 1: s_j = scale * <q_h, K_j>, softmax, weighted sum of V_j),
+ * the online-softmax update of the (m, l, acc) state, s10.1 (one CTA serves
+ * all g query heads of a KV head and reads each K/V tile once), s10.2 and
+ * s9.1 (the history is split into NP partitions whose states are merged
+ * exactly: M = max m_p, out = sum_p acc_p e^(m_p - M) / sum_p l_p e^(m_p - M)).
+ *
+ *   q            [B][Hq][D] bf16 (the prologue's q_out)
+ *   out_f32      [B][Hq][D] float, nullable
+ *   out_bf16     [B][Hq][D] bf16 (nearest-even cast of the fp32 result), nullable
+ *   workspace    device scratch of ws_bytes >= decode_attn_workspace_size(...)
+ *                (may be NULL when that size is 0); contents need no
+ *                initialisation; concurrent calls must not share it.
+ *   num_partitions  0 = automatic, else the requested NP.
+ * A sequence with T_b = 0 produces zeros.
+ */
+int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+                      const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
+                      int Hkv, int D, int page_size, int max_pages, int num_pages, float scale,
+                      int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
+                      size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * attn_partition_merge -- exact merge of NP partition states (s9.1).
+ *   m, l  [B][Hq][NP] float   running max of the scores (natural-log units)
+ *                             and the softmax denominator, both relative to m
+ *   acc   [B][Hq][NP][D]      unnormalised weighted sums of V relative to m
+ *   out = sum_p acc_p e^(m_p - M) / sum_p l_p e^(m_p - M), M = max_p m_p;
+ *   zeros when the denominator is 0. Empty partitions (m = -1e30, l = 0,
+ *   acc = 0) contribute nothing. 1 <= NP <= 65536.
+ */
+int attn_partition_merge(const float *m, const float *l, const float *acc, int B, int Hq, int D,
+                         int NP, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream);
+
+/*
+ * Host-tiled variant ("EdgeTransformerEngine", KV-offload design): the
+ * state (m, l, acc) lives in global memory across KV tiles, so device memory
+ * for KV is constant in the context length.
+ *   m, l  [B][Hq] float, acc [B][Hq][D] float (natural-log units as above).
+ *
+ * attn_tile_init     m = -1e30, l = 0, acc = 0.
+ * attn_tile_update   fold one tile of n_pos (1..512) consecutive positions
+ *                    into the state with the online-softmax update:
+ *                    k_tile, v_tile [B][n_pos][Hkv][D] bf16, q [B][Hq][D] bf16.
+ * attn_tile_finalize out = acc / l (zeros where l = 0).
+ */
+int attn_tile_init(float *m, float *l, float *acc, int B, int Hq, int D, cudaStream_t stream);
+int attn_tile_update(const pgqa_bf16 *q, const pgqa_bf16 *k_tile, const pgqa_bf16 *v_tile,
+                     int n_pos, int B, int Hq, int Hkv, int D, float scale, float *m, float *l,
+                     float *acc, cudaStream_t stream);
+int attn_tile_finalize(const float *m, const float *l, const float *acc, int B, int Hq, int D,
+                       float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream);
+
+/*
+ * attn_host_tiled_run -- enqueue the whole host-tiled attention: init, then
+ * for each tile t of tile_len positions (the last may be shorter) a copy of
+ * K and V from pinned host memory into device slot s = t % n_slots on
+ * copy_stream, then attn_tile_update on compute_stream, then finalize.
+ * Two event dependencies per slot order the slots (copy_done[s]: data ready
+ * before it is read; compute_done[s]: slot free before it is overwritten),
+ * so copies of later tiles overlap the update of earlier ones.
+ *
+ *   host_k, host_v  [B][T][Hkv][D] bf16, pinned host memory
+ *   k_slots, v_slots  host arrays of n_slots device pointers, each slot
+ *                     [B][tile_len][Hkv][D] bf16; 2 <= n_slots <= 8
+ *   events          host array of 2 * n_slots caller-created events
+ *                   (copy_done[0..n_slots), then compute_done[0..n_slots))
+ *   tile_len        1..512
+ * Returns after enqueueing; the output is ready when compute_stream reaches
+ * the end of the enqueued work. The streams must differ.
+ */
+int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
+                        int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
+                        int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
+                        cudaEvent_t const *events, float *m, float *l, float *acc,
+                        float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
+                        cudaStream_t copy_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGQA_H */

@@ -1,0 +1,404 @@
+// api.cu -- the C ABI of libpgqa (declared in include/pgqa.h): argument
+// validation, partition choice and launch. Every entry point returns a status
+// code and records a message for pgqa_last_error(); none throws, allocates or
+// synchronises (except pgqa_device_error, which reads the device flags).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include <atomic>
+
+#include "launch.h"
+#include "pgqa.h"
+
+namespace pgqa {
+constexpr int kHeadDimHost = 128;
+}
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok()
+{
+    g_last_error[0] = '\0';
+    return PGQA_OK;
+}
+
+int cuda_fail(cudaError_t err, const char *where)
+{
+    return fail(PGQA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Shape checks common to every attention entry point. Returns 0 or a status.
+int check_heads(const char *fn, int B, int Hq, int Hkv, int D)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need B >= 0, Hq > 0, Hkv > 0 (got %d, %d, %d)", fn, B,
+                    Hq, Hkv);
+    if (B > 65535)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: B = %d exceeds 65535", fn, B);
+    if (D != pgqa::kHeadDimHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: head dim %d unsupported (only 128)", fn, D);
+    if (Hq % Hkv != 0)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: Hq = %d is not a multiple of Hkv = %d", fn, Hq, Hkv);
+    const int g = Hq / Hkv;
+    if (g < 1 || g > 8)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: group size Hq/Hkv = %d outside [1, 8]", fn, g);
+    return 0;
+}
+
+int check_pages(const char *fn, int page_size, int max_pages, int num_pages)
+{
+    if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: page_size %d is not a power of two in [16, 256]", fn,
+                    page_size);
+    if (max_pages < 0 || num_pages < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: negative max_pages or num_pages", fn);
+    if (static_cast<long long>(max_pages) * page_size > 0x7FFFFFFFLL)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: max_pages * page_size exceeds 2^31 - 1", fn);
+    return 0;
+}
+
+int sm_count_current_device()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 0;
+    if (dev < 64) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0)
+            return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev < 64)
+        cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *pgqa_last_error(void) { return g_last_error; }
+
+int pgqa_device_error(unsigned *flags_out, int clear)
+{
+    if (!flags_out)
+        return fail(PGQA_ERR_INVALID_ARG, "pgqa_device_error: flags_out is NULL");
+    cudaError_t err = cudaDeviceSynchronize();
+    if (err != cudaSuccess)
+        return cuda_fail(err, "pgqa_device_error");
+    unsigned a = 0, b = 0;
+    if ((err = pgqa::read_flags_prologue(&a, clear != 0)) != cudaSuccess)
+        return cuda_fail(err, "pgqa_device_error");
+    if ((err = pgqa::read_flags_decode(&b, clear != 0)) != cudaSuccess)
+        return cuda_fail(err, "pgqa_device_error");
+    *flags_out = a | b;
+    return ok();
+}
+
+int qk_norm_rope_append(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                        const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                        const int32_t *context_lens, const int32_t *block_table,
+                        pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq,
+                        int Hkv, int D, int page_size, int max_pages, int num_pages,
+                        float rope_theta, float eps, cudaStream_t stream)
+{
+    const char *fn = "qk_norm_rope_append";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (int st = check_pages(fn, page_size, max_pages, num_pages))
+        return st;
+    if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: rope_theta must be > 0 and eps >= 0", fn);
+    if (B == 0)
+        return ok();
+    if (!q || !k || !v || !gamma_q || !gamma_k || !context_lens || !block_table || !k_cache ||
+        !v_cache || !q_out)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gamma_q) ||
+        !aligned16(gamma_k) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_out) ||
+        !aligned4(context_lens) || !aligned4(block_table))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
+    pgqa::PrologueArgs a{q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache,
+                         q_out, B, Hq, Hkv, page_size, max_pages, num_pages,
+                         static_cast<double>(rope_theta), eps};
+    cudaError_t err = pgqa::launch_prologue(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int decode_attn_partition_count(int B, int Hkv, int page_size, int max_pages, int num_partitions)
+{
+    if (B < 0 || Hkv <= 0 || page_size <= 0 || max_pages < 0 || num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "decode_attn_partition_count: invalid arguments");
+    return pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                   sm_count_current_device());
+}
+
+size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                  int num_partitions)
+{
+    (void)D;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || page_size <= 0 || max_pages < 0 || num_partitions < 0)
+        return 0;
+    const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                           sm_count_current_device());
+    return pgqa::decode_workspace_bytes(B, Hq, np);
+}
+
+int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+                      const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
+                      int Hkv, int D, int page_size, int max_pages, int num_pages, float scale,
+                      int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
+                      size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "decode_attn_paged";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (int st = check_pages(fn, page_size, max_pages, num_pages))
+        return st;
+    if (num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
+    if (!std::isfinite(scale))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (B == 0)
+        return ok();
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!out_f32 && !out_bf16)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: out_f32 and out_bf16 are both NULL", fn);
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) ||
+        !aligned4(block_table) || !aligned4(context_lens) || (workspace && !aligned16(workspace)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
+    const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                           sm_count_current_device());
+    const size_t need = pgqa::decode_workspace_bytes(B, Hq, np);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu",
+                    fn, need, np, workspace ? ws_bytes : static_cast<size_t>(0));
+    pgqa::DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.num_partitions = np;
+    a.pages_per_part = max_pages > 0 ? (max_pages + np - 1) / np : 1;
+    a.out_f32 = out_f32;
+    a.out_bf16 = out_bf16;
+    a.ws = static_cast<float *>(workspace);
+    cudaError_t err = pgqa::launch_decode(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int attn_partition_merge(const float *m, const float *l, const float *acc, int B, int Hq, int D,
+                         int NP, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream)
+{
+    const char *fn = "attn_partition_merge";
+    if (B < 0 || Hq <= 0 || NP < 1)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need B >= 0, Hq > 0, NP >= 1", fn);
+    if (NP > pgqa::kMaxPartitions)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: NP = %d exceeds %d", fn, NP, pgqa::kMaxPartitions);
+    if (D != pgqa::kHeadDimHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: head dim %d unsupported (only 128)", fn, D);
+    if (static_cast<long long>(B) * Hq > 0x7FFFFFFFLL)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: B * Hq too large", fn);
+    if (B == 0)
+        return ok();
+    if (!m || !l || !acc || (!out_f32 && !out_bf16))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned4(m) || !aligned4(l) || !aligned16(acc) || (out_f32 && !aligned16(out_f32)) ||
+        (out_bf16 && !aligned16(out_bf16)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: acc/out need 16-byte, m/l 4-byte alignment", fn);
+    pgqa::MergeArgs a{};
+    a.m = m;
+    a.l = l;
+    a.acc = acc;
+    a.B = B;
+    a.Hq = Hq;
+    a.NP = NP;
+    a.out_f32 = out_f32;
+    a.out_bf16 = out_bf16;
+    cudaError_t err = pgqa::launch_merge(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int attn_tile_init(float *m, float *l, float *acc, int B, int Hq, int D, cudaStream_t stream)
+{
+    const char *fn = "attn_tile_init";
+    if (B < 0 || Hq <= 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need B >= 0, Hq > 0", fn);
+    if (D != pgqa::kHeadDimHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: head dim %d unsupported (only 128)", fn, D);
+    if (B == 0)
+        return ok();
+    if (!m || !l || !acc)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned4(m) || !aligned4(l) || !aligned16(acc))
+        return fail(PGQA_ERR_MISALIGNED, "%s: acc needs 16-byte, m/l 4-byte alignment", fn);
+    cudaError_t err = pgqa::launch_tile_init(m, l, acc, B, Hq, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int attn_tile_update(const pgqa_bf16 *q, const pgqa_bf16 *k_tile, const pgqa_bf16 *v_tile,
+                     int n_pos, int B, int Hq, int Hkv, int D, float scale, float *m, float *l,
+                     float *acc, cudaStream_t stream)
+{
+    const char *fn = "attn_tile_update";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (n_pos < 0 || n_pos > 512)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: n_pos = %d outside [0, 512]", fn, n_pos);
+    if (!std::isfinite(scale))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (B == 0 || n_pos == 0)
+        return ok();
+    if (!q || !k_tile || !v_tile || !m || !l || !acc)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned16(q) || !aligned16(k_tile) || !aligned16(v_tile) || !aligned4(m) || !aligned4(l) ||
+        !aligned16(acc))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte, m/l 4-byte alignment", fn);
+    pgqa::TileArgs a{q, k_tile, v_tile, n_pos, B, Hq, Hkv, scale, m, l, acc};
+    cudaError_t err = pgqa::launch_tile_update(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int attn_tile_finalize(const float *m, const float *l, const float *acc, int B, int Hq, int D,
+                       float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream)
+{
+    const char *fn = "attn_tile_finalize";
+    if (B < 0 || Hq <= 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need B >= 0, Hq > 0", fn);
+    if (D != pgqa::kHeadDimHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: head dim %d unsupported (only 128)", fn, D);
+    if (B == 0)
+        return ok();
+    if (!l || !acc || (!out_f32 && !out_bf16))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned4(l) || !aligned16(acc) || (out_f32 && !aligned16(out_f32)) ||
+        (out_bf16 && !aligned16(out_bf16)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte, l 4-byte alignment", fn);
+    cudaError_t err = pgqa::launch_tile_finalize(m, l, acc, B, Hq, out_f32, out_bf16, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
+                        int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
+                        int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
+                        cudaEvent_t const *events, float *m, float *l, float *acc,
+                        float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
+                        cudaStream_t copy_stream)
+{
+    const char *fn = "attn_host_tiled_run";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (T < 0 || tile_len < 1 || tile_len > 512 || n_slots < 2 || n_slots > 8)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need T >= 0, tile_len in [1, 512], n_slots in [2, 8]", fn);
+    if (compute_stream == copy_stream)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: compute and copy streams must differ", fn);
+    if (B == 0)
+        return ok();
+    if (!q || (T > 0 && (!host_k || !host_v)) || !k_slots || !v_slots || !events || !m || !l ||
+        !acc || (!out_f32 && !out_bf16))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    for (int s = 0; s < n_slots; ++s) {
+        if (!k_slots[s] || !v_slots[s] || !events[s] || !events[n_slots + s])
+            return fail(PGQA_ERR_INVALID_ARG, "%s: slot %d has a NULL buffer or event", fn, s);
+        if (!aligned16(k_slots[s]) || !aligned16(v_slots[s]))
+            return fail(PGQA_ERR_MISALIGNED, "%s: slot %d is not 16-byte aligned", fn, s);
+    }
+    if (!aligned16(q) || !aligned16(host_k) || !aligned16(host_v))
+        return fail(PGQA_ERR_MISALIGNED, "%s: q and the host K/V need 16-byte alignment", fn);
+
+    int st = attn_tile_init(m, l, acc, B, Hq, D, compute_stream);
+    if (st != PGQA_OK)
+        return st;
+    const cudaEvent_t *copy_done = events;
+    const cudaEvent_t *compute_done = events + n_slots;
+    cudaError_t err;
+    // No copy may land in a slot before the compute stream's earlier work
+    // (which may still read the slots) is done.
+    if ((err = cudaEventRecord(compute_done[0], compute_stream)) != cudaSuccess ||
+        (err = cudaStreamWaitEvent(copy_stream, compute_done[0], 0)) != cudaSuccess)
+        return cuda_fail(err, "attn_host_tiled_run: initial stream ordering");
+    const size_t pos_bytes = static_cast<size_t>(Hkv) * D * sizeof(pgqa_bf16);
+    const int n_tiles = (T + tile_len - 1) / tile_len;
+    for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % n_slots;
+        const int t0 = t * tile_len;
+        const int n_pos = T - t0 < tile_len ? T - t0 : tile_len;
+        // The slot is free once the update that last read it has finished.
+        if (t >= n_slots && (err = cudaStreamWaitEvent(copy_stream, compute_done[s], 0)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(copy)");
+        // Host rows of sequence b are [b][t0 .. t0+n_pos); the slot holds
+        // [b][0 .. n_pos) packed: a 2-D copy with one row per sequence.
+        const size_t row_bytes = static_cast<size_t>(n_pos) * pos_bytes;
+        const size_t src_pitch = static_cast<size_t>(T) * pos_bytes;
+        const size_t dst_pitch = row_bytes;
+        const char *hk = reinterpret_cast<const char *>(host_k) + static_cast<size_t>(t0) * pos_bytes;
+        const char *hv = reinterpret_cast<const char *>(host_v) + static_cast<size_t>(t0) * pos_bytes;
+        if (B == 1) {
+            err = cudaMemcpyAsync(k_slots[s], hk, row_bytes, cudaMemcpyHostToDevice, copy_stream);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(v_slots[s], hv, row_bytes, cudaMemcpyHostToDevice, copy_stream);
+        } else {
+            err = cudaMemcpy2DAsync(k_slots[s], dst_pitch, hk, src_pitch, row_bytes, B,
+                                    cudaMemcpyHostToDevice, copy_stream);
+            if (err == cudaSuccess)
+                err = cudaMemcpy2DAsync(v_slots[s], dst_pitch, hv, src_pitch, row_bytes, B,
+                                        cudaMemcpyHostToDevice, copy_stream);
+        }
+        if (err != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: tile copy");
+        if ((err = cudaEventRecord(copy_done[s], copy_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(copy)");
+        if ((err = cudaStreamWaitEvent(compute_stream, copy_done[s], 0)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(compute)");
+        st = attn_tile_update(q, k_slots[s], v_slots[s], n_pos, B, Hq, Hkv, D, scale, m, l, acc,
+                              compute_stream);
+        if (st != PGQA_OK)
+            return st;
+        if ((err = cudaEventRecord(compute_done[s], compute_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(compute)");
+    }
+    return attn_tile_finalize(m, l, acc, B, Hq, D, out_f32, out_bf16, compute_stream);
+}
+
+} // extern "C"

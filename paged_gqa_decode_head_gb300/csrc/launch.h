@@ -1,0 +1,74 @@
+// launch.h -- host-side launchers of the libpgqa kernels (internal).
+// The C ABI in api.cu validates arguments and then calls these.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "pgqa.h"
+
+namespace pgqa {
+
+struct PrologueArgs {
+    const pgqa_bf16 *q, *k, *v, *gamma_q, *gamma_k;
+    const int32_t *context_lens, *block_table;
+    pgqa_bf16 *k_cache, *v_cache, *q_out;
+    int B, Hq, Hkv, page_size, max_pages, num_pages;
+    double rope_theta;
+    float eps;
+};
+
+struct DecodeArgs {
+    const pgqa_bf16 *q, *k_cache, *v_cache;
+    const int32_t *block_table, *context_lens;
+    int B, Hq, Hkv, page_size, max_pages, num_pages;
+    float scale;
+    int num_partitions;  // NP >= 1 (already resolved)
+    int pages_per_part;  // ceil(max_pages / NP)
+    float *out_f32;      // nullable
+    pgqa_bf16 *out_bf16; // nullable
+    float *ws;           // partial states when NP > 1
+};
+
+struct MergeArgs {
+    const float *m, *l, *acc;
+    int B, Hq, NP;
+    float *out_f32;
+    pgqa_bf16 *out_bf16;
+    // When context_lens is non-null, sequence b uses only its first
+    // ceil(ceil(T_b / page_size) / pages_per_part) partitions and m is in
+    // base-2 units (the decode kernel's private workspace format).
+    const int32_t *context_lens;
+    int page_size, pages_per_part, max_pages;
+};
+
+struct TileArgs {
+    const pgqa_bf16 *q, *k_tile, *v_tile;
+    int n_pos, B, Hq, Hkv;
+    float scale;
+    float *m, *l, *acc;
+};
+
+// Largest partition count the merge supports.
+constexpr int kMaxPartitions = 65536;
+
+cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
+cudaError_t launch_tile_init(float *m, float *l, float *acc, int B, int Hq, cudaStream_t stream);
+cudaError_t launch_tile_update(const TileArgs &a, cudaStream_t stream);
+cudaError_t launch_tile_finalize(const float *m, const float *l, const float *acc, int B, int Hq,
+                                 float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream);
+
+// Partition choice shared by decode_attn_paged and its workspace query.
+int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requested, int sm_count);
+size_t decode_workspace_bytes(int B, int Hq, int num_partitions);
+
+// Each translation unit keeps its own sticky device flag word; these read
+// (and optionally clear) it synchronously on the current device.
+cudaError_t read_flags_prologue(unsigned *flags, bool clear);
+cudaError_t read_flags_decode(unsigned *flags, bool clear);
+
+} // namespace pgqa

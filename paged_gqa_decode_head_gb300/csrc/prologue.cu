@@ -1,0 +1,166 @@
+// prologue.cu -- fused per-head Q/K RMSNorm + half-rotation RoPE + paged K/V
+// append for the decode step.
+//
+// "From Qwen3 math to CUDA kernels: a 0.6B inference runtime":
+//   s2.3 per-head RMSNorm of Q and K with learned gains (s2.1: eps), V is
+//        not normalised;
+//   s2.4 RoPE rotates the pair (x_i, x_{i+D/2}) by pos * theta^(-2i/D);
+//   s7.1 one warp per head: lane l holds dims l, l+32, l+64, l+96, so both
+//        RoPE pairs (l, l+64) and (l+32, l+96) are in-lane and the norm is
+//        a 5-step shuffle reduction;
+//   s7.2 the rotated K goes straight to its physical page
+//        block_table[b][pos / P] at offset pos % P.
+//
+// The RoPE phase pos * omega_i is formed in fp64 (omega_i is computed on the
+// host in fp64) and reduced modulo 2*pi before the fp32 sincosf, so the angle
+// stays accurate to ~1e-7 rad even at pos ~ 1e5 where an fp32 product would
+// be off by ~1e-2 rad.
+#include "common.cuh"
+#include "launch.h"
+
+namespace pgqa {
+namespace {
+
+__device__ unsigned g_flags_prologue;
+
+constexpr int kWarpsPerBlock = 4;
+constexpr int kHalf = kHeadDim / 2;
+
+struct PrologueParams {
+    const uint16_t *q, *k, *v, *gamma_q, *gamma_k;
+    const int32_t *context_lens, *block_table;
+    uint16_t *k_cache, *v_cache, *q_out;
+    int B, Hq, Hkv, P, max_pages, num_pages;
+    float eps;
+    double inv_freq[kHalf]; // theta^(-2i/D), i < D/2
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
+{
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Rotate the pair (a, b) of frequency index i at position pos.
+__device__ __forceinline__ void rope_pair(float &a, float &b, int pos, double inv_freq)
+{
+    // 2*pi as an unevaluated sum hi + lo of two doubles.
+    constexpr double kTwoPiHi = 6.283185307179586232;
+    constexpr double kTwoPiLo = 2.4492935982947064e-16;
+    constexpr double kInvTwoPi = 0.15915494309189535;
+    const double phi = static_cast<double>(pos) * inv_freq;
+    const double n = rint(phi * kInvTwoPi);
+    double r = fma(-n, kTwoPiHi, phi);
+    r = fma(-n, kTwoPiLo, r);
+    float sn, cs;
+    sincosf(static_cast<float>(r), &sn, &cs);
+    const float ra = a * cs - b * sn;
+    const float rb = b * cs + a * sn;
+    a = ra;
+    b = rb;
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int heads = p.Hq + p.Hkv;
+    const int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (item >= p.B * heads)
+        return;
+    const int b = item / heads;
+    const int hh = item % heads;
+    const int T = p.context_lens[b];
+    if (T < 1 || T > p.max_pages * p.P) {
+        if (hh == 0 && lane == 0)
+            atomicOr(&g_flags_prologue, PGQA_DEVERR_BAD_CONTEXT);
+        return;
+    }
+    const int pos = T - 1;
+    const bool is_q = hh < p.Hq;
+    const int h = is_q ? hh : hh - p.Hq;
+
+    const uint16_t *src;
+    const uint16_t *gamma;
+    uint16_t *dst;
+    if (is_q) {
+        src = p.q + (static_cast<size_t>(b) * p.Hq + h) * kHeadDim;
+        gamma = p.gamma_q;
+        dst = p.q_out + (static_cast<size_t>(b) * p.Hq + h) * kHeadDim;
+    } else {
+        const int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + pos / p.P];
+        if (phys < 0 || phys >= p.num_pages) {
+            if (lane == 0)
+                atomicOr(&g_flags_prologue, PGQA_DEVERR_BAD_PAGE);
+            return;
+        }
+        const size_t slot = ((static_cast<size_t>(phys) * p.Hkv + h) * p.P + pos % p.P) * kHeadDim;
+        src = p.k + (static_cast<size_t>(b) * p.Hkv + h) * kHeadDim;
+        gamma = p.gamma_k;
+        dst = p.k_cache + slot;
+        // V is appended bit for bit: 32 lanes x 8 bytes = one 256-byte row.
+        const uint2 *vrow = reinterpret_cast<const uint2 *>(p.v + (static_cast<size_t>(b) * p.Hkv + h) * kHeadDim);
+        reinterpret_cast<uint2 *>(p.v_cache + slot)[lane] = vrow[lane];
+    }
+
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        x[i] = bf16_bits_to_f32(src[lane + 32 * i]);
+    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+    const float inv_rms = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        x[i] = x[i] * inv_rms * bf16_bits_to_f32(gamma[lane + 32 * i]);
+    // pairs (lane, lane + 64) and (lane + 32, lane + 96)
+    rope_pair(x[0], x[2], pos, p.inv_freq[lane]);
+    rope_pair(x[1], x[3], pos, p.inv_freq[lane + 32]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        dst[lane + 32 * i] = f32_to_bf16_bits(x[i]);
+}
+
+} // namespace
+
+cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
+{
+    if (a.B == 0)
+        return cudaSuccess;
+    PrologueParams p{};
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.gamma_q = a.gamma_q;
+    p.gamma_k = a.gamma_k;
+    p.context_lens = a.context_lens;
+    p.block_table = a.block_table;
+    p.k_cache = a.k_cache;
+    p.v_cache = a.v_cache;
+    p.q_out = a.q_out;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.P = a.page_size;
+    p.max_pages = a.max_pages;
+    p.num_pages = a.num_pages;
+    p.eps = a.eps;
+    for (int i = 0; i < kHalf; ++i)
+        p.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / kHeadDim);
+    const long items = static_cast<long>(a.B) * (a.Hq + a.Hkv);
+    const unsigned blocks = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    prologue_kernel<<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t read_flags_prologue(unsigned *flags, bool clear)
+{
+    cudaError_t err = cudaMemcpyFromSymbol(flags, g_flags_prologue, sizeof(unsigned));
+    if (err == cudaSuccess && clear) {
+        const unsigned zero = 0;
+        err = cudaMemcpyToSymbol(g_flags_prologue, &zero, sizeof(unsigned));
+    }
+    return err;
+}
+
+} // namespace pgqa

@@ -27,7 +27,7 @@ import numpy as np
 BF16_NAN = np.uint16(0xFFFF)
 UNUSED_TABLE_ENTRY = np.int32(0x3FFFFFFF)
 
-_CHUNK = 1 << 24
+_CHUNK = 1 << 20
 
 
 def generator(seed: int, stream: int) -> np.random.Generator:
@@ -46,12 +46,24 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
 
 
 def normal_bf16(gen: np.random.Generator, shape) -> np.ndarray:
-    """bf16 bit patterns of N(0, 1) draws, generated in chunks."""
+    """bf16 bit patterns of N(0, 1) draws. Generated through one reused chunk
+    buffer (large fresh temporaries are slow to fault in on some hosts)."""
     n = int(np.prod(shape, dtype=np.int64))
     out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, _CHUNK):
-        e = min(n, s + _CHUNK)
-        out[s:e] = f32_to_bf16_bits(gen.standard_normal(e - s, dtype=np.float32))
+    chunk = max(1, min(n, _CHUNK))
+    f = np.empty(chunk, dtype=np.float32)
+    u = f.view(np.uint32)
+    t = np.empty(chunk, dtype=np.uint32)
+    for s in range(0, n, chunk):
+        m = min(n, s + chunk) - s
+        gen.standard_normal(out=f[:m], dtype=np.float32)
+        # nearest-even rounding to the top 16 bits, as in f32_to_bf16_bits
+        np.right_shift(u[:m], np.uint32(16), out=t[:m])
+        np.bitwise_and(t[:m], np.uint32(1), out=t[:m])
+        np.add(t[:m], np.uint32(0x7FFF), out=t[:m])
+        np.add(t[:m], u[:m], out=t[:m])
+        np.right_shift(t[:m], np.uint32(16), out=t[:m])
+        out[s:s + m] = t[:m]
     return out.reshape(shape)
 
 
@@ -187,3 +199,51 @@ WORKLOADS = {
                                 partition=512, outlier_fraction=0.01, outlier_factor=8.0),
     "host_tiled_t64k": dict(seed=1004, B=1, Hq=16, Hkv=8, D=128, T=65536, tile=512),
 }
+
+
+# ---------------------------------------------------------------- workload builders
+def qwen3_layers(layers: int | None = None, T: int | None = None):
+    """Qwen3-0.6B-shaped decode: per layer a paged cache of T positions
+    (Hkv=8, D=128, P=16, random block table over its own pool) and a new token
+    (Hq=16). Returns [(PagedKV, NewToken)] * layers."""
+    w = WORKLOADS["qwen3_0p6b_t8k"]
+    L = w["layers"] if layers is None else layers
+    T = w["T"] if T is None else T
+    out = []
+    for i in range(L):
+        seed = w["seed"] * 1000 + i
+        kv = paged_kv(seed, [T] * w["B"], Hkv=w["Hkv"], D=w["D"], page_size=w["page_size"], spare_pages=0,
+                      fill_unused="normal")
+        tok = new_token(seed, w["B"], w["Hq"], w["Hkv"], w["D"])
+        out.append((kv, tok))
+    return out
+
+
+def ragged_b64():
+    """Batched ragged decode: B=64, T_b ~ U[1, 32768], one shared page pool."""
+    w = WORKLOADS["ragged_b64"]
+    ctx = ragged_lengths(w["seed"], w["B"], w["T_lo"], w["T_hi"])
+    max_pages = (w["T_hi"] + w["page_size"] - 1) // w["page_size"]
+    kv = paged_kv(w["seed"], ctx, Hkv=w["Hkv"], D=w["D"], page_size=w["page_size"], max_pages=max_pages,
+                  fill_unused="normal")
+    q = query(w["seed"], w["B"], w["Hq"], w["D"])
+    return kv, q
+
+
+def long_split_kv():
+    """Long-context split-KV: B=1, Hq=32, Hkv=8, T=131072, keys at 1% of the
+    positions multiplied by 8 (written straight into the cache)."""
+    w = WORKLOADS["long_split_kv_t128k"]
+    kv = paged_kv(w["seed"], [w["T"]], Hkv=w["Hkv"], D=w["D"], page_size=w["page_size"], spare_pages=0,
+                  fill_unused="normal")
+    scale_key_outliers(kv, w["seed"], w["outlier_fraction"], w["outlier_factor"])
+    q = query(w["seed"], w["B"], w["Hq"], w["D"])
+    return kv, q
+
+
+def host_tiled_kv():
+    """Host-tiled offload: B=1, Hq=16, Hkv=8, T=65536 history [B, T, Hkv, D]."""
+    w = WORKLOADS["host_tiled_t64k"]
+    k, v = contiguous_kv(w["seed"], w["B"], w["T"], w["Hkv"], w["D"])
+    q = query(w["seed"], w["B"], w["Hq"], w["D"])
+    return q, k, v

@@ -209,6 +209,37 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
                         float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
                         cudaStream_t copy_stream);
 
+/*
+ * decode_attn_paged_static -- decode_attn_paged for callers that cannot
+ * allocate device memory. The pages have no counterpart of this entry point;
+ * it exists for code that runs where cudaMalloc is not allowed (inside an
+ * allocator or memory-pool callback, in a plugin whose host owns all device
+ * memory, in a loop that forbids allocation after start-up) and so cannot
+ * provide decode_attn_paged's workspace.
+ *
+ * Same arguments and results as decode_attn_paged, without the workspace:
+ * the partition scratch is a fixed array of PGQA_STATIC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until the
+ * process exits. Sizes whose scratch (decode_attn_workspace_size) exceeds it
+ * are refused with PGQA_ERR_WORKSPACE and a message naming both sizes.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *
+ * The first call on each device (that needs scratch) looks the array's
+ * device address up with cudaGetSymbolAddress; make that first call before
+ * any stream capture on that device. All calls share the one array, which
+ * keeps the last call's contents; no part of it has to start at zero, but
+ * calls whose work overlaps on the GPU (different streams, or no ordering
+ * between them) race on it and must not be issued.
+ */
+#define PGQA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+int decode_attn_paged_static(const pgqa_bf16 *q, const pgqa_bf16 *k_cache,
+                             const pgqa_bf16 *v_cache, const int32_t *block_table,
+                             const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                             int page_size, int max_pages, int num_pages, float scale,
+                             int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                             cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

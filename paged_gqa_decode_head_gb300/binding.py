@@ -32,6 +32,7 @@ EXPORTED = (
     "attn_tile_update",
     "attn_tile_finalize",
     "attn_host_tiled_run",
+    "decode_attn_paged_static",
 )
 
 STATUS_NAMES = {
@@ -91,6 +92,8 @@ def load_library():
         lib.attn_tile_finalize.restype = I
         lib.attn_host_tiled_run.argtypes = [P, P, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P, P, P, P]
         lib.attn_host_tiled_run.restype = I
+        lib.decode_attn_paged_static.argtypes = [P] * 5 + [I] * 7 + [F, I, P, P, P]
+        lib.decode_attn_paged_static.restype = I
         _lib = lib
         return lib
 
@@ -252,3 +255,23 @@ def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, event
         _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
         _stream(compute_stream), _stream(copy_stream))
     _check("attn_host_tiled_run", st)
+
+
+STATIC_SCRATCH_BYTES = 8 << 20  # PGQA_STATIC_SCRATCH_BYTES in include/pgqa.h
+
+
+def decode_attn_paged_static(q, k_cache, v_cache, block_table, context_lens, scale: float, out_f32=None,
+                             out_bf16=None, num_partitions: int = 0, stream=None) -> None:
+    """decode_attn_paged without a workspace, for callers that cannot allocate:
+    the partition scratch is the library's built-in array (see include/pgqa.h)."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_cache.shape
+    st = lib.decode_attn_paged_static(
+        _dev(q, bf, "q"), _dev(k_cache, bf, "k_cache"), _dev(v_cache, bf, "v_cache"),
+        _dev(block_table, i32, "block_table"), _dev(context_lens, i32, "context_lens"), B, Hq, Hkv, D, P,
+        block_table.shape[1], num_pages, float(scale), int(num_partitions),
+        _dev(out_f32, torch.float32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
+        _stream(stream))
+    _check("decode_attn_paged_static", st)

@@ -94,6 +94,15 @@ int sm_count_current_device()
 
 } // namespace
 
+int pgqa::report_error(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 extern "C" {
 
 const char *pgqa_last_error(void) { return g_last_error; }

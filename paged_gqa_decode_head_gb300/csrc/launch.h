@@ -71,4 +71,7 @@ size_t decode_workspace_bytes(int B, int Hq, int num_partitions);
 cudaError_t read_flags_prologue(unsigned *flags, bool clear);
 cudaError_t read_flags_decode(unsigned *flags, bool clear);
 
+// Record a message for pgqa_last_error() and return `code` (printf format).
+int report_error(int code, const char *fmt, ...);
+
 } // namespace pgqa

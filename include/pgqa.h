@@ -142,8 +142,19 @@ size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, 
  *   out_f32      [B][Hq][D] float, nullable
  *   out_bf16     [B][Hq][D] bf16 (nearest-even cast of the fp32 result), nullable
  *   workspace    device scratch of ws_bytes >= decode_attn_workspace_size(...)
- *                (may be NULL when that size is 0); contents need no
- *                initialisation; concurrent calls must not share it.
+ *                (may be NULL when that size is 0). Zero-fill it before the
+ *                first call with given (B, Hq, Hkv, num_partitions, page_size,
+ *                max_pages); every call that completes leaves it ready for
+ *                the next call with the same arguments (its partition
+ *                tickets back at zero). Calls whose work may overlap on the
+ *                GPU must not share a workspace.
+ * Launch and ordering: the kernels are launched with programmatic stream
+ * serialisation. The attention kernel may start before the previous kernel
+ * in the stream has finished and then already reads block_table,
+ * context_lens and the cache rows of positions below T_b - 1; only q and the
+ * row of position T_b - 1 (written by qk_norm_rope_append) are read after
+ * that kernel completes. The previous kernel must therefore not write those
+ * inputs (qk_norm_rope_append does not).
  *   num_partitions  0 = automatic, else the requested NP.
  * A sequence with T_b = 0 produces zeros.
  */
@@ -227,9 +238,10 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
  * The first call on each device (that needs scratch) looks the array's
  * device address up with cudaGetSymbolAddress; make that first call before
  * any stream capture on that device. All calls share the one array, which
- * keeps the last call's contents; no part of it has to start at zero, but
- * calls whose work overlaps on the GPU (different streams, or no ordering
- * between them) race on it and must not be issued.
+ * keeps the last call's contents: each call first clears the part that must
+ * start at zero (the partition tickets) with cudaMemsetAsync on `stream`.
+ * Calls whose work overlaps on the GPU (different streams, or no ordering
+ * between them) race on the array and must not be issued.
  */
 #define PGQA_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 

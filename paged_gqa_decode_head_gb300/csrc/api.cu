@@ -171,7 +171,7 @@ size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, 
         return 0;
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    return pgqa::decode_workspace_bytes(B, Hq, np);
+    return pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
 }
 
 int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
@@ -189,6 +189,8 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
         return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
     if (!std::isfinite(scale))
         return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (static_cast<long long>(num_pages) * Hkv * page_size > 0x7FFFFFFFLL)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: num_pages * Hkv * page_size exceeds 2^31 - 1 rows", fn);
     if (B == 0)
         return ok();
     if (!q || !k_cache || !v_cache || !block_table || !context_lens)
@@ -201,7 +203,7 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    const size_t need = pgqa::decode_workspace_bytes(B, Hq, np);
+    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
     if (need > 0 && (!workspace || ws_bytes < need))
         return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu",
                     fn, need, np, workspace ? ws_bytes : static_cast<size_t>(0));

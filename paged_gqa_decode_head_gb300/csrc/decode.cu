@@ -5,23 +5,41 @@
 //   s10.1 one CTA per (sequence, KV head) serves all g query heads of the
 //         group, so every K/V byte is read from HBM once;
 //   s10.2 the history is cut into partitions, one CTA each, whose
-//         (m_p, l_p, o_p) go to a preallocated fp32 scratch, and a second
-//         launch merges them;
+//         (m_p, l_p, o_p) go to a preallocated fp32 scratch and are merged;
 //   s9.1  the merge rescales every partition to the common maximum, which is
 //         exact (not an approximation);
-//   s12.1 / s12.2 multi-stage prefetch, 16-byte aligned copies, masked tails.
+//   s12.1 / s12.2 multi-stage prefetch, aligned copies, masked tails,
+//         swizzled shared memory against bank conflicts.
 //
-// GB300 design. Grid = (partition, KV head, sequence). Each of the CTA's 4
-// warps owns every 4th 16-key chunk of the partition and a private ring of 3
-// shared-memory stages; lane 0 of the warp looks the chunk's physical page up
-// in the block table and issues two 4 KiB bulk TMA copies (K rows, V rows:
-// the rows of one page and KV head are contiguous) that complete on the
-// stage's mbarrier. The warp folds each staged chunk into its (m, l, acc)
-// (attn_core.cuh) and refills the stage with the chunk 3 ahead. At the end the
-// warps' states are merged through shared memory; NP = 1 writes the output,
-// NP > 1 writes the partition state and the merge kernel finishes.
+// GB300 design.
+// * Grid = (partition, KV head, sequence), one 288-thread CTA per SM. Each of
+//   the 9 warps owns every 9th 16-position chunk of the partition and a
+//   private ring of 3 shared-memory stages (27 chunks = 216 KiB per CTA). Lane
+//   0 issues four 2-D TMA loads per chunk (K and V, dims 0-63 and 64-127, 16
+//   rows each, 128-byte swizzle) that complete on the stage's mbarrier.
+// * The warp folds its resident chunks together with tensor-core MMAs
+//   (mma.sync m16n8k16, bf16 in, fp32 accumulate), transposed so the g <= 8
+//   query heads fill the N = 8 columns: S^T = K Q^T, the online softmax on the
+//   S^T fragments, then O^T += V^T P^T with P split into bf16 hi + lo parts
+//   (~16 significant bits). ldmatrix reads the swizzled tiles without bank
+//   conflicts; movmatrix turns P^T from the accumulator layout into the B
+//   operand layout.
+// * Programmatic dependent launch: a partition's first chunks are requested
+//   before griddepcontrol.wait, so one layer's history streams in while the
+//   previous kernels in the stream (the previous layer, this layer's prologue)
+//   finish; the query and the chunk holding the new token are read after it.
+//   With 27 chunks per SM a whole 8192-position, 8-head layer fits.
+// * The warps' states are merged in shared memory; NP = 1 writes the output,
+//   NP > 1 writes the partition state. With at most kFusedMergeMax
+//   partitions the last CTA of each (sequence, KV head) to finish (a ticket
+//   counter in the workspace, reset by that CTA) merges them; the others exit
+//   at once, freeing their SM for the next layer. Larger NP use merge_kernel
+//   (also launched with programmatic dependence).
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "attn_core.cuh"
 #include "launch.h"
@@ -33,44 +51,334 @@ __device__ unsigned g_flags_decode;
 
 __device__ __forceinline__ void raise_flag(unsigned f) { atomicOr(&g_flags_decode, f); }
 
-constexpr int kWarps = 4;
+// One CTA per SM holding 27 staged chunks (216 KiB): across 152 SMs that is
+// more than a whole 8192-position layer of one 8-head KV cache.
+constexpr int kWarps = 9;
 constexpr int kStages = 3;
-constexpr int kStageBytes = 2 * kChunkBytes; // K chunk then V chunk
-constexpr int kCtasPerSm = 2;                // what the shared-memory footprint allows
-constexpr int kSplitSmem = kWarps * kStages * kStageBytes + kWarps * kStages * 8;
+constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
+constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
+constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
+constexpr int kSplitSmem = 1024 /* alignment slack */ + kWarps * kStages * kStageBytes +
+                           kWarps * kStages * 8 /* mbarriers */ +
+                           kWarps * kStages * 4 /* valid rows per stage */ + 16 /* ticket */;
 
 struct SplitParams {
-    const __nv_bfloat16 *q;
-    const char *k_cache, *v_cache;
+    const uint16_t *q;
     const int32_t *block_table, *context_lens;
     float *out_f32;
     uint16_t *out_bf16;
     float *ws_m, *ws_l, *ws_acc;
+    unsigned *tickets; // [B*Hkv] partition tickets (fused merge)
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
+    int fused_merge;
     float scale_log2;
 };
 
-template <int G>
-__global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitParams p)
+__device__ __forceinline__ uint32_t ld_u32(const uint16_t *p)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+
+// Per-warp online-softmax state on mma fragments, computed transposed so the
+// g <= 8 query heads fill the mma's N = 8 columns instead of padding its M =
+// 16 rows: S^T = K Q^T (A = 16 keys x 16 dims of K, B = Q^T) and
+// O^T += V^T P^T (A = 16 dims x 16 keys of V^T, B = P^T). Lane (g, t) =
+// (lane / 4, lane % 4) holds heads 2t and 2t+1 (valid when < G) for keys g
+// and g+8 of a chunk, and O^T rows (dims) 16mt+g and 16mt+g+8.
+template <int G> struct MmaWarp {
+    uint32_t qb0[8], qb1[8]; // B = Q^T: head g, dims 16ks+2t..+1 and 16ks+8+2t..+1 (bf16x2)
+    float o[8][4];           // O^T m-tile mt: [dim 16mt+g][2t], [..][2t+1], [dim 16mt+g+8][2t], [..][2t+1]
+    float m[2];              // running max of heads 2t, 2t+1 (base-2 units)
+    float l[2];              // sum of p of heads 2t, 2t+1 over this lane's keys
+
+    __device__ __forceinline__ void init(const uint16_t *q_rows)
+    {
+        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            qb0[ks] = g < G ? ld_u32(q_rows + g * kHeadDim + 16 * ks + 2 * t) : 0u;
+            qb1[ks] = g < G ? ld_u32(q_rows + g * kHeadDim + 16 * ks + 8 + 2 * t) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        m[0] = m[1] = kEmptyMax;
+        l[0] = l[1] = 0.f;
+    }
+
+    // Fold NC resident chunks at once (their MMAs and loads interleave):
+    // stage[c] is the shared address of chunk c's four swizzled boxes and
+    // rows[c] (1..16) its valid rows; later rows are masked out.
+    template <int NC>
+    __device__ __forceinline__ void fold(const uint32_t (&stage)[kStages], const int (&rows)[kStages],
+                                         float scale_log2)
+    {
+        const int lane = threadIdx.x & 31, g = lane >> 2;
+        const int mq = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row within it
+
+        // S^T = K Q^T over 8 k-steps of 16 dims, two accumulators per chunk
+        // (even and odd k-steps) to shorten the dependent MMA chains.
+        float sa[NC][4], sb[NC][4];
+#pragma unroll
+        for (int c = 0; c < NC; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sa[c][e] = sb[c][e] = 0.f;
+        const int k_key = ((mq & 1) << 3) + mr;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const int unit = (2 * ks + (mq >> 1)) & 7;
+            const uint32_t off = (ks >> 2) * kBoxBytes + k_key * 128 + ((unit ^ mr) << 4);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                uint32_t a[4];
+                ldmatrix_x4(a, stage[c] + off);
+                mma_bf16_16816((ks & 1) ? sb[c] : sa[c], a, qb0[ks], qb1[ks]);
+            }
+        }
+        // sc[c][e]: e = 0 (key g, head 2t), 1 (key g, 2t+1), 2 (key g+8, 2t), 3 (key g+8, 2t+1)
+        float sc[NC][4];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[c][e] = (sa[c][e] + sb[c][e]) * scale_log2;
+            if (g >= rows[c])
+                sc[c][0] = sc[c][1] = -INFINITY;
+            if (g + 8 >= rows[c])
+                sc[c][2] = sc[c][3] = -INFINITY;
+        }
+        float mn[2];
+        bool grow = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float cm = fmaxf(sc[0][h], sc[0][2 + h]);
+#pragma unroll
+            for (int c = 1; c < NC; ++c)
+                cm = fmaxf(cm, fmaxf(sc[c][h], sc[c][2 + h]));
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 4));
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 8));
+            cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, 16));
+            mn[h] = fmaxf(m[h], cm);
+            grow |= mn[h] > m[h];
+        }
+        if (__any_sync(0xFFFFFFFFu, grow)) {
+            const float c0 = exp2f(m[0] - mn[0]), c1 = exp2f(m[1] - mn[1]);
+            l[0] *= c0;
+            l[1] *= c1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= c0;
+                o[mt][2] *= c0;
+                o[mt][1] *= c1;
+                o[mt][3] *= c1;
+            }
+            m[0] = mn[0];
+            m[1] = mn[1];
+        }
+        // P^T as bf16 hi + lo (hi carries 8 significant bits, lo the next 8),
+        // transposed from the accumulator layout into the B operand layout.
+        uint32_t bh0[NC], bh1[NC], bl0[NC], bl1[NC];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                p[e] = exp2f(sc[c][e] - m[e & 1]); // masked: exp2(-inf) = 0
+            l[0] += p[0] + p[2];
+            l[1] += p[1] + p[3];
+            const uint32_t hi0 = pack_bf16x2(p[0], p[1]), hi1 = pack_bf16x2(p[2], p[3]);
+            const uint32_t lo0 = pack_bf16x2(p[0] - bf16_lo(hi0), p[1] - bf16_hi(hi0));
+            const uint32_t lo1 = pack_bf16x2(p[2] - bf16_lo(hi1), p[3] - bf16_hi(hi1));
+            bh0[c] = movmatrix_trans(hi0);
+            bh1[c] = movmatrix_trans(hi1);
+            bl0[c] = movmatrix_trans(lo0);
+            bl1[c] = movmatrix_trans(lo1);
+        }
+        const int v_key = ((mq >> 1) << 3) + mr;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int dtile = 2 * mt + (mq & 1); // 8-dim block this lane addresses
+            const uint32_t off =
+                2 * kBoxBytes + (dtile >> 3) * kBoxBytes + v_key * 128 + (((dtile & 7) ^ mr) << 4);
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, stage[c] + off);
+                mma_bf16_16816(o[mt], a, bh0[c], bh1[c]);
+                mma_bf16_16816(o[mt], a, bl0[c], bl1[c]);
+            }
+        }
+    }
+
+    // Warp totals: reduce l over the 8 lanes sharing t; write the record
+    // [G][128] O, then [G] m, then [G] l.
+    __device__ __forceinline__ void store_record(float *rec)
+    {
+        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            l[c] += __shfl_xor_sync(0xFFFFFFFFu, l[c], 4);
+            l[c] += __shfl_xor_sync(0xFFFFFFFFu, l[c], 8);
+            l[c] += __shfl_xor_sync(0xFFFFFFFFu, l[c], 16);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int h = 2 * t + c;
+            if (h < G) {
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    rec[h * kHeadDim + 16 * mt + g] = o[mt][c];
+                    rec[h * kHeadDim + 16 * mt + g + 8] = o[mt][2 + c];
+                }
+                if (g == 0) {
+                    rec[G * kHeadDim + h] = m[c];
+                    rec[G * kHeadDim + G + h] = l[c];
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void clear()
+    {
+        m[0] = m[1] = kEmptyMax;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+};
+
+// The last CTA of a (sequence, KV head) to finish merges the n (2..64)
+// partition states of its G query heads from the workspace (base-2 m) and
+// writes the outputs: one warp per head reduces M and L with shuffles, then
+// every thread folds its share of the acc rows, 8 independent loads at a time.
+template <int G>
+__device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, float *scratch)
+{
+    constexpr int kThreads = kWarps * 32;
+    float *w = scratch;                 // [G][kFusedMergeMax] weights e^(m_p - M)
+    float *Ls = w + G * kFusedMergeMax; // [G], padded to 16 floats
+    float *red = Ls + 16;               // [kThreads] float4 partial sums
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
+    for (int h = warp; h < G; h += kWarps) {
+        const float *mh = p.ws_m + (row0 + h) * p.NP;
+        const float *lh = p.ws_l + (row0 + h) * p.NP;
+        const float m0 = lane < n ? __ldcg(mh + lane) : kEmptyMax;
+        const float m1 = lane + 32 < n ? __ldcg(mh + lane + 32) : kEmptyMax;
+        const float l0 = lane < n ? __ldcg(lh + lane) : 0.f;
+        const float l1 = lane + 32 < n ? __ldcg(lh + lane + 32) : 0.f;
+        float M = fmaxf(m0, m1);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+        const float w0 = exp2f(m0 - M), w1 = exp2f(m1 - M);
+        float L = l0 * w0 + l1 * w1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            L += __shfl_xor_sync(0xFFFFFFFFu, L, off);
+        w[h * kFusedMergeMax + lane] = w0;
+        w[h * kFusedMergeMax + lane + 32] = w1;
+        if (lane == 0)
+            Ls[h] = L;
+    }
+    __syncthreads();
+    constexpr int kItems = G * 32; // (head, 4 dims)
+    constexpr int kSlices = kThreads >= kItems ? kThreads / kItems : 1;
+    constexpr int kLanesPerSlice = kThreads / kSlices;
+    constexpr int kRound = 8;
+    for (int base = 0; base < kItems; base += kLanesPerSlice) {
+        const int item = base + (threadIdx.x % kLanesPerSlice);
+        const int slice = threadIdx.x / kLanesPerSlice;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (item < kItems && slice < kSlices) {
+            const int h = item / 32, d4 = item % 32;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.ws_acc + (row0 + h) * p.NP * kHeadDim) + d4;
+            for (int i0 = slice; i0 < n; i0 += kRound * kSlices) {
+                float4 v[kRound];
+#pragma unroll
+                for (int i = 0; i < kRound; ++i) {
+                    const int part = i0 + i * kSlices;
+                    v[i] = part < n ? __ldcg(src + static_cast<size_t>(part) * (kHeadDim / 4))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int i = 0; i < kRound; ++i) {
+                    const int part = i0 + i * kSlices;
+                    const float wt = part < n ? w[h * kFusedMergeMax + part] : 0.f;
+                    acc.x = fmaf(v[i].x, wt, acc.x);
+                    acc.y = fmaf(v[i].y, wt, acc.y);
+                    acc.z = fmaf(v[i].z, wt, acc.z);
+                    acc.w = fmaf(v[i].w, wt, acc.w);
+                }
+            }
+        }
+        reinterpret_cast<float4 *>(red)[threadIdx.x] = acc;
+        __syncthreads();
+        if (slice == 0 && item < kItems) {
+            float4 sum = acc;
+            for (int sl = 1; sl < kSlices; ++sl) {
+                const float4 v = reinterpret_cast<const float4 *>(red)[threadIdx.x + sl * kLanesPerSlice];
+                sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
+            }
+            const int h = item / 32, d4 = item % 32;
+            const float L = Ls[h];
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float r[4] = {sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv};
+            const size_t off = (row0 + h) * kHeadDim + 4 * d4;
+            if (p.out_f32)
+                *reinterpret_cast<float4 *>(p.out_f32 + off) = make_float4(r[0], r[1], r[2], r[3]);
+            if (p.out_bf16)
+                *reinterpret_cast<uint2 *>(p.out_bf16 + off) =
+                    make_uint2(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]));
+        }
+        __syncthreads();
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const SplitParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int part = blockIdx.x;
     const int kvh = blockIdx.y;
     const int b = blockIdx.z;
 
+    allow_dependent_launch();
+
+    const int part_tokens = p.ppp * p.P;
+    const int tok0 = part * part_tokens;
+    const int32_t *table = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    auto chunk_token = [&](int k) { return tok0 + (warp + k * kWarps) * kChunkTokens; };
+    // The first 32 table entries of this warp's chunks are loaded before the
+    // context length is known (any entry below max_pages may be read), so the
+    // two loads overlap.
+    int tbl_blk = 0;
+    int tbl_val;
+    {
+        const int page = chunk_token(lane) / p.P;
+        tbl_val = (chunk_token(lane) < tok0 + part_tokens && page < p.max_pages) ? table[page] : -1;
+    }
     int T = p.context_lens[b];
     if (T < 0 || T > p.max_pages * p.P) {
         if (part == 0 && threadIdx.x == 0)
             raise_flag(PGQA_DEVERR_BAD_CONTEXT);
         T = 0;
     }
-    const int part_tokens = p.ppp * p.P;
     const int n_parts = max(1, (T + part_tokens - 1) / part_tokens);
-    if (part >= n_parts)
-        return; // this sequence is shorter than the launch's longest
-    const int tok0 = part * part_tokens;
+    if (part >= n_parts) {
+        grid_dependency_wait(); // keep the chain ordered even when idle
+        return;
+    }
     const int tok1 = min(T, tok0 + part_tokens);
     const int n_chunks = max(0, (tok1 - tok0 + kChunkTokens - 1) / kChunkTokens);
     const int my_chunks = (n_chunks > warp) ? (n_chunks - 1 - warp) / kWarps + 1 : 0;
@@ -78,6 +386,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitPa
     unsigned char *stages = smem + warp * kStages * kStageBytes;
     uint64_t *bars =
         reinterpret_cast<uint64_t *>(smem + kWarps * kStages * kStageBytes) + warp * kStages;
+    int *stage_rows =
+        reinterpret_cast<int *>(smem + kWarps * kStages * kStageBytes + kWarps * kStages * 8) +
+        warp * kStages;
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < kStages; ++s)
@@ -86,55 +397,116 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitPa
     }
     __syncwarp();
 
-    const int32_t *table = p.block_table + static_cast<size_t>(b) * p.max_pages;
-    // k-th chunk of this warp starts at token tok0 + (warp + k*kWarps)*16, which
-    // never straddles a page because page_size is a multiple of 16.
-    auto chunk_token = [&](int k) { return tok0 + (warp + k * kWarps) * kChunkTokens; };
-    auto issue = [&](int k, uint64_t policy) {
+    // The chunk holding position T-1 is written by the prologue this kernel
+    // may overlap, so it is requested only after griddepcontrol.wait.
+    auto holds_new_token = [&](int k) { return chunk_token(k) + kChunkTokens > T - 1; };
+    // Physical pages of this warp's chunks, 32 at a time: lane L caches the
+    // entry of chunk 32*blk + L. Called by the whole (converged) warp.
+    auto phys_of = [&](int k) {
+        if ((k >> 5) != tbl_blk) {
+            tbl_blk = k >> 5;
+            const int kk = (tbl_blk << 5) + lane;
+            tbl_val = kk < my_chunks ? table[chunk_token(kk) / p.P] : -1;
+        }
+        return __shfl_sync(0xFFFFFFFFu, tbl_val, k & 31);
+    };
+    // Lane 0 requests chunk k (phys from phys_of) and records its valid rows.
+    auto issue = [&](int k, int phys, uint64_t policy) {
         const int t = chunk_token(k);
-        const int phys = table[t / p.P];
         uint64_t *bar = &bars[k % kStages];
         if (phys < 0 || phys >= p.num_pages) {
             raise_flag(PGQA_DEVERR_BAD_PAGE);
+            stage_rows[k % kStages] = 0;
             mbar_arrive(bar); // complete the phase with no data; the keys are masked
             return;
         }
-        const size_t row0 = (static_cast<size_t>(phys) * p.Hkv + kvh) * p.P + (t % p.P);
+        stage_rows[k % kStages] = min(kChunkTokens, tok1 - t);
+        const int row = (phys * p.Hkv + kvh) * p.P + (t % p.P);
         unsigned char *dst = stages + (k % kStages) * kStageBytes;
         mbar_arrive_expect_tx(bar, kStageBytes);
-        bulk_copy_g2s(dst, p.k_cache + row0 * kRowBytes, kChunkBytes, bar, policy);
-        bulk_copy_g2s(dst + kChunkBytes, p.v_cache + row0 * kRowBytes, kChunkBytes, bar, policy);
+        tma_load_2d(dst, &tmap_k, 0, row, bar, policy);
+        tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, bar, policy);
+        tma_load_2d(dst + 2 * kBoxBytes, &tmap_v, 0, row, bar, policy);
+        tma_load_2d(dst + 3 * kBoxBytes, &tmap_v, 64, row, bar, policy);
     };
 
-    uint64_t policy = 0;
+    const uint64_t policy = l2_evict_first_policy();
+    const int first = min(kStages, my_chunks);
+    int first_phys[kStages];
+#pragma unroll
+    for (int k = 0; k < kStages; ++k)
+        first_phys[k] = k < first ? phys_of(k) : -1;
     if (lane == 0) {
-        policy = l2_evict_first_policy();
-        const int first = min(kStages, my_chunks);
-        for (int k = 0; k < first; ++k)
-            issue(k, policy);
+#pragma unroll
+        for (int k = 0; k < kStages; ++k)
+            if (k < first && !holds_new_token(k))
+                issue(k, first_phys[k], policy);
     }
+    grid_dependency_wait();
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kStages; ++k)
+            if (k < first && holds_new_token(k))
+                issue(k, first_phys[k], policy);
+    }
+    __syncwarp();
 
-    WarpAttn<G> st;
-    st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim, p.scale_log2);
+    MmaWarp<G> st;
+    st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
 
-    int k = 0;
+    // Chunks are consumed in groups of up to kStages (one per stage); the
+    // group's stages are refilled together once it has been folded.
     bool ok = true;
-    for (; k < my_chunks; ++k) {
-        const int s = k % kStages;
-        const bool landed = mbar_wait_bounded(&bars[s], (k / kStages) & 1);
-        if (!__all_sync(0xFFFFFFFFu, landed)) { // keep the warp's lanes in step
-            ok = false;
-            break;
+    int k0 = 0;
+    for (; k0 < my_chunks; k0 += kStages) {
+        const int nc = min(kStages, my_chunks - k0);
+        uint32_t stage_addr[kStages];
+        int rows[kStages];
+#pragma unroll
+        for (int c = 0; c < kStages; ++c) {
+            const int k = k0 + c;
+            stage_addr[c] = smem_addr(stages + (k % kStages) * kStageBytes);
+            rows[c] = 0;
+            if (c < nc) {
+                const bool landed = mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1);
+                if (!__all_sync(0xFFFFFFFFu, landed))
+                    ok = false;
+                rows[c] = stage_rows[k % kStages];
+                if (rows[c] < kChunkTokens) {
+                    // Rows past the history (all rows of a chunk whose page
+                    // was refused) may hold anything, even NaN: zero their V
+                    // so that p = 0 times V stays 0 in the MMA.
+                    unsigned char *stage = stages + (k % kStages) * kStageBytes;
+                    const int n_units = (kChunkTokens - rows[c]) * 16;
+                    for (int u = lane; u < n_units; u += 32) {
+                        const int row = rows[c] + u / 16;
+                        const int box = 2 + ((u >> 3) & 1);
+                        *reinterpret_cast<uint4 *>(stage + box * kBoxBytes + row * 128 + (u & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
+            }
         }
-        const int t = chunk_token(k);
-        const int phys = table[t / p.P];
-        const int n_valid = (phys >= 0 && phys < p.num_pages) ? min(kChunkTokens, tok1 - t) : 0;
-        const uint32_t a = smem_addr(stages + s * kStageBytes);
-        st.fold_chunk(SmemRows{a, a + kChunkBytes}, n_valid);
+        if (!ok)
+            break;
+        if (nc == 3)
+            st.template fold<3>(stage_addr, rows, p.scale_log2);
+        else if (nc == 2)
+            st.template fold<2>(stage_addr, rows, p.scale_log2);
+        else
+            st.template fold<1>(stage_addr, rows, p.scale_log2);
         __syncwarp();
-        if (lane == 0 && k + kStages < my_chunks) {
-            fence_proxy_async_smem();
-            issue(k + kStages, policy);
+#pragma unroll
+        for (int c = 0; c < kStages; ++c) {
+            const int k = k0 + c + kStages;
+            if (k < my_chunks) {
+                const int phys = phys_of(k);
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issue(k, phys, policy);
+                }
+            }
         }
     }
     if (!ok) {
@@ -142,27 +514,18 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitPa
         // still in flight into this warp's stages, and contribute nothing.
         if (lane == 0)
             raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
-        const int issued = min(my_chunks, k + kStages);
-        for (int kk = k; kk < issued; ++kk)
+        const int issued = min(my_chunks, k0 + kStages);
+        for (int kk = k0; kk < issued; ++kk)
             (void)mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            st.m[h] = kEmptyMax;
-            st.l[h] = 0.f;
-#pragma unroll
-            for (int e = 0; e < WarpAttn<G>::DPL; ++e)
-                st.acc[h][e] = 0.f;
-        }
+        st.clear();
     }
 
-    st.reduce_groups();
     __syncwarp();
-    // Every copy into this warp's stages has landed, so the stages can hold
-    // the warp's state record.
+    // Every copy into this warp's stages has landed: they can hold its record.
     st.store_record(reinterpret_cast<float *>(stages));
     __syncthreads();
 
-    const int base_q = kvh * G;
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
     for (int e = threadIdx.x; e < G * kHeadDim; e += kWarps * 32) {
         const int h = e / kHeadDim;
         const int d = e % kHeadDim;
@@ -180,7 +543,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitPa
             L = fmaf(rec[G * kHeadDim + G + h], wt, L);
             O = fmaf(rec[h * kHeadDim + d], wt, O);
         }
-        const size_t row = static_cast<size_t>(b) * p.Hq + base_q + h;
+        const size_t row = row0 + h;
         if (n_parts == 1) {
             const float o = L > 0.f ? O / L : 0.f;
             if (p.out_f32)
@@ -196,6 +559,26 @@ __global__ void __launch_bounds__(kWarps * 32) decode_split_kernel(const SplitPa
             p.ws_acc[idx * kHeadDim + d] = O;
         }
     }
+    if (n_parts == 1 || !p.fused_merge)
+        return;
+
+    // Ticket: the CTA that finishes last for this (sequence, KV head) merges.
+    // The barrier orders every thread's partial-state stores before thread
+    // 0's release; its acquire (when last) orders the other CTAs' stores
+    // before the merge's loads, which the second barrier extends to all
+    // threads.
+    unsigned *ticket_slot = reinterpret_cast<unsigned *>(
+        smem + kWarps * kStages * kStageBytes + kWarps * kStages * 8 + kWarps * kStages * 4);
+    __syncthreads();
+    unsigned *ticket = p.tickets + static_cast<size_t>(b) * p.Hkv + kvh;
+    if (threadIdx.x == 0)
+        *ticket_slot = atomic_add_acq_rel_gpu(ticket, 1u);
+    __syncthreads();
+    if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
+        return;
+    merge_in_last_cta<G>(p, b, kvh, n_parts, reinterpret_cast<float *>(smem));
+    if (threadIdx.x == 0)
+        *ticket = 0u; // ready for the next call
 }
 
 struct MergeParams {
@@ -209,19 +592,24 @@ struct MergeParams {
 
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeRound = 8; // partitions per warp whose loads are in flight together
 
-// One CTA per (sequence, query head). Pass 1 finds M = max_p m_p; pass 2 has
-// warp w accumulate partitions w, w+8, ... with lane i owning dims 4i..4i+3;
-// the 8 warps' sums are then combined in shared memory.
+// One CTA per (sequence, query head). Warp w folds partitions w, w+8, ...,
+// kMergeRound at a time: all loads of a round are issued before any is used,
+// and the round is folded into the warp's running (M, L, O) like the online
+// softmax update (lane i owns dims 4i..4i+3). The 8 warps' states are then
+// merged through shared memory.
 template <bool kBase2>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p)
 {
-    __shared__ float red_max[kMergeWarps];
+    __shared__ float red_m[kMergeWarps];
     __shared__ float red_l[kMergeWarps];
     __shared__ float4 red_o[kMergeWarps][32];
     const int row = blockIdx.x; // b * Hq + h
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    allow_dependent_launch();
+    grid_dependency_wait();
     int np = p.NP;
     if (p.context_lens) {
         const int b = row / p.Hq;
@@ -236,47 +624,58 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const float *m = p.m + static_cast<size_t>(row) * p.NP;
     const float *l = p.l + static_cast<size_t>(row) * p.NP;
     const float4 *acc = reinterpret_cast<const float4 *>(p.acc + static_cast<size_t>(row) * p.NP * kHeadDim);
+    const float to_base2 = kBase2 ? 1.f : kLog2e;
 
-    float M = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += kMergeThreads)
-        M = fmaxf(M, __ldcg(m + i));
+    float M = kEmptyMax, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i0 = warp; i0 < np; i0 += kMergeWarps * kMergeRound) {
+        float mi[kMergeRound], li[kMergeRound];
+        float4 ai[kMergeRound];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-    if (lane == 0)
-        red_max[warp] = M;
-    __syncthreads();
-    M = red_max[0];
+        for (int r = 0; r < kMergeRound; ++r) {
+            const int i = i0 + r * kMergeWarps;
+            const bool in = i < np;
+            mi[r] = in ? __ldcg(m + i) * to_base2 : kEmptyMax;
+            li[r] = in ? __ldcg(l + i) : 0.f;
+            ai[r] = in ? __ldcg(acc + static_cast<size_t>(i) * (kHeadDim / 4) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float mn = M;
 #pragma unroll
-    for (int w = 1; w < kMergeWarps; ++w)
-        M = fmaxf(M, red_max[w]);
-    if (M == -INFINITY)
-        M = 0.f; // every m is -inf: all weights become 0
-
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = warp; i < np; i += kMergeWarps) {
-        const float mi = __ldcg(m + i);
-        const float wt = kBase2 ? exp2f(mi - M) : expf(mi - M);
-        L = fmaf(__ldcg(l + i), wt, L);
-        const float4 a = __ldcg(acc + static_cast<size_t>(i) * (kHeadDim / 4) + lane);
-        o.x = fmaf(a.x, wt, o.x);
-        o.y = fmaf(a.y, wt, o.y);
-        o.z = fmaf(a.z, wt, o.z);
-        o.w = fmaf(a.w, wt, o.w);
+        for (int r = 0; r < kMergeRound; ++r)
+            mn = fmaxf(mn, mi[r]);
+        const float corr = exp2f(M - mn);
+        L *= corr;
+        O.x *= corr, O.y *= corr, O.z *= corr, O.w *= corr;
+#pragma unroll
+        for (int r = 0; r < kMergeRound; ++r) {
+            const float wt = exp2f(mi[r] - mn);
+            L = fmaf(li[r], wt, L);
+            O.x = fmaf(ai[r].x, wt, O.x);
+            O.y = fmaf(ai[r].y, wt, O.y);
+            O.z = fmaf(ai[r].z, wt, O.z);
+            O.w = fmaf(ai[r].w, wt, O.w);
+        }
+        M = mn;
     }
-    red_o[warp][lane] = o;
-    if (lane == 0)
+    red_o[warp][lane] = O;
+    if (lane == 0) {
+        red_m[warp] = M;
         red_l[warp] = L;
+    }
     __syncthreads();
     if (threadIdx.x < kHeadDim) {
         const int d = threadIdx.x;
+        float Mt = red_m[0];
+#pragma unroll
+        for (int w = 1; w < kMergeWarps; ++w)
+            Mt = fmaxf(Mt, red_m[w]);
         float Ls = 0.f, Os = 0.f;
 #pragma unroll
         for (int w = 0; w < kMergeWarps; ++w) {
-            Ls += red_l[w];
-            Os += reinterpret_cast<const float *>(&red_o[w][0])[d];
+            const float wt = exp2f(red_m[w] - Mt);
+            Ls = fmaf(red_l[w], wt, Ls);
+            Os = fmaf(reinterpret_cast<const float *>(&red_o[w][0])[d], wt, Os);
         }
         const float out = Ls > 0.f ? Os / Ls : 0.f;
         if (p.out_f32)
@@ -288,7 +687,46 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
 constexpr int kMaxDevices = 64;
 
-template <int G> cudaError_t launch_split(const SplitParams &kp, dim3 grid, cudaStream_t stream)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D map over a paged cache seen as [num_pages * Hkv * P rows][128 bf16]:
+// boxes of 16 rows x 64 columns, 128-byte swizzle.
+cudaError_t encode_cache_map(CUtensorMap *map, const void *base, long long rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kChunkTokens)};
+    const cuuint32_t elem[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int G>
+cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
+                         dim3 grid, cudaStream_t stream)
 {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
@@ -296,16 +734,17 @@ template <int G> cudaError_t launch_split(const SplitParams &kp, dim3 grid, cuda
     if (err != cudaSuccess)
         return err;
     if (dev >= kMaxDevices || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kSplitSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < kMaxDevices)
             configured[dev] = true;
     }
-    decode_split_kernel<G><<<grid, kWarps * 32, kSplitSmem, stream>>>(kp);
-    return cudaGetLastError();
+    return launch_pdl(decode_mma_kernel<G>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk, mv, kp);
 }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 } // namespace
 
@@ -333,23 +772,37 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
     return static_cast<int>((max_pages + ppp - 1) / ppp);
 }
 
-static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+size_t decode_ticket_bytes(int B, int Hkv)
+{
+    return align256(static_cast<size_t>(B) * Hkv * sizeof(unsigned));
+}
 
-size_t decode_workspace_bytes(int B, int Hq, int num_partitions)
+// Workspace (NP > 1): partition tickets [B*Hkv] (zero before first use;
+// every completed call leaves them zero), then m, l [B*Hq*NP] and acc
+// [B*Hq*NP*128] (fp32, no initial value needed).
+size_t decode_workspace_bytes(int B, int Hkv, int Hq, int num_partitions)
 {
     if (num_partitions <= 1)
         return 0;
     const size_t n = static_cast<size_t>(B) * Hq * num_partitions;
-    return 2 * align256(n * sizeof(float)) + align256(n * kHeadDim * sizeof(float));
+    return decode_ticket_bytes(B, Hkv) + 2 * align256(n * sizeof(float)) +
+           align256(n * kHeadDim * sizeof(float));
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
 {
     const int G = a.Hq / a.Hkv;
+    CUtensorMap mk, mv;
+    const long long rows = static_cast<long long>(a.num_pages) * a.Hkv * a.page_size;
+    if (rows == 0)
+        return cudaErrorInvalidValue;
+    cudaError_t err = encode_cache_map(&mk, a.k_cache, rows);
+    if (err == cudaSuccess)
+        err = encode_cache_map(&mv, a.v_cache, rows);
+    if (err != cudaSuccess)
+        return err;
     SplitParams kp{};
-    kp.q = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-    kp.k_cache = reinterpret_cast<const char *>(a.k_cache);
-    kp.v_cache = reinterpret_cast<const char *>(a.v_cache);
+    kp.q = a.q;
     kp.block_table = a.block_table;
     kp.context_lens = a.context_lens;
     kp.out_f32 = a.out_f32;
@@ -362,27 +815,29 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
+    kp.fused_merge = a.num_partitions <= kFusedMergeMax ? 1 : 0;
     if (a.num_partitions > 1) {
         const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;
         char *ws = reinterpret_cast<char *>(a.ws);
+        kp.tickets = reinterpret_cast<unsigned *>(ws);
+        ws += decode_ticket_bytes(a.B, a.Hkv);
         kp.ws_m = reinterpret_cast<float *>(ws);
         kp.ws_l = reinterpret_cast<float *>(ws + align256(n * sizeof(float)));
         kp.ws_acc = reinterpret_cast<float *>(ws + 2 * align256(n * sizeof(float)));
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
-    cudaError_t err;
     switch (G) {
-    case 1: err = launch_split<1>(kp, grid, stream); break;
-    case 2: err = launch_split<2>(kp, grid, stream); break;
-    case 3: err = launch_split<3>(kp, grid, stream); break;
-    case 4: err = launch_split<4>(kp, grid, stream); break;
-    case 5: err = launch_split<5>(kp, grid, stream); break;
-    case 6: err = launch_split<6>(kp, grid, stream); break;
-    case 7: err = launch_split<7>(kp, grid, stream); break;
-    case 8: err = launch_split<8>(kp, grid, stream); break;
+    case 1: err = launch_split<1>(mk, mv, kp, grid, stream); break;
+    case 2: err = launch_split<2>(mk, mv, kp, grid, stream); break;
+    case 3: err = launch_split<3>(mk, mv, kp, grid, stream); break;
+    case 4: err = launch_split<4>(mk, mv, kp, grid, stream); break;
+    case 5: err = launch_split<5>(mk, mv, kp, grid, stream); break;
+    case 6: err = launch_split<6>(mk, mv, kp, grid, stream); break;
+    case 7: err = launch_split<7>(mk, mv, kp, grid, stream); break;
+    case 8: err = launch_split<8>(mk, mv, kp, grid, stream); break;
     default: return cudaErrorInvalidValue;
     }
-    if (err != cudaSuccess || a.num_partitions <= 1)
+    if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)
         return err;
     MergeArgs ma{};
     ma.m = kp.ws_m;
@@ -418,10 +873,8 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream)
     mp.max_pages = a.max_pages;
     const unsigned rows = static_cast<unsigned>(a.B) * a.Hq;
     if (a.context_lens)
-        merge_kernel<true><<<rows, kMergeThreads, 0, stream>>>(mp);
-    else
-        merge_kernel<false><<<rows, kMergeThreads, 0, stream>>>(mp);
-    return cudaGetLastError();
+        return launch_pdl(merge_kernel<true>, dim3(rows), dim3(kMergeThreads), 0, stream, mp);
+    return launch_pdl(merge_kernel<false>, dim3(rows), dim3(kMergeThreads), 0, stream, mp);
 }
 
 cudaError_t read_flags_decode(unsigned *flags, bool clear)

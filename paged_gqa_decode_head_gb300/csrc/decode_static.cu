@@ -69,11 +69,20 @@ extern "C" int decode_attn_paged_static(const pgqa_bf16 *q, const pgqa_bf16 *k_c
             need, kStaticScratchBytes);
     void *scratch = nullptr;
     if (need > 0) {
-        const cudaError_t err = scratch_address(&scratch);
+        cudaError_t err = scratch_address(&scratch);
         if (err != cudaSuccess)
             return pgqa::report_error(PGQA_ERR_CUDA,
                                       "decode_attn_paged_static: cudaGetSymbolAddress failed: %s",
                                       cudaGetErrorString(err));
+        // The array keeps whatever the last call left, and a call with other
+        // sizes may have left partition data where this call's partition
+        // tickets go; they must start at zero.
+        if (B > 0 && Hkv > 0) {
+            err = cudaMemsetAsync(scratch, 0, pgqa::decode_ticket_bytes(B, Hkv), stream);
+            if (err != cudaSuccess)
+                return pgqa::report_error(PGQA_ERR_CUDA, "decode_attn_paged_static: clearing tickets: %s",
+                                          cudaGetErrorString(err));
+        }
     }
     return decode_attn_paged(q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
                              page_size, max_pages, num_pages, scale, num_partitions, out_f32,

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -64,12 +65,34 @@ cudaError_t launch_tile_finalize(const float *m, const float *l, const float *ac
 
 // Partition choice shared by decode_attn_paged and its workspace query.
 int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requested, int sm_count);
-size_t decode_workspace_bytes(int B, int Hq, int num_partitions);
+size_t decode_workspace_bytes(int B, int Hkv, int Hq, int num_partitions);
+// Bytes at the start of that workspace holding the partition tickets.
+size_t decode_ticket_bytes(int B, int Hkv);
 
 // Each translation unit keeps its own sticky device flag word; these read
 // (and optionally clear) it synchronously on the current device.
 cudaError_t read_flags_prologue(unsigned *flags, bool clear);
 cudaError_t read_flags_decode(unsigned *flags, bool clear);
+
+// Launch `kernel` on `stream` with programmatic stream serialisation: it may
+// start while the previous kernel in the stream is still running, and must
+// call griddepcontrol.wait before touching anything that kernel produces.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Record a message for pgqa_last_error() and return `code` (printf format).
 int report_error(int code, const char *fmt, ...);

@@ -61,6 +61,10 @@ __device__ __forceinline__ void rope_pair(float &a, float &b, int pos, double in
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
 {
+    // Everything this kernel reads may come from the kernel before it, and
+    // what it writes may still be read there: wait before touching memory.
+    allow_dependent_launch();
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int heads = p.Hq + p.Hkv;
     const int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
@@ -149,8 +153,7 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
         p.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / kHeadDim);
     const long items = static_cast<long>(a.B) * (a.Hq + a.Hkv);
     const unsigned blocks = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    prologue_kernel<<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(prologue_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
 }
 
 cudaError_t read_flags_prologue(unsigned *flags, bool clear)

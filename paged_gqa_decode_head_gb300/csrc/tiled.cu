@@ -21,6 +21,8 @@ constexpr int kTileWarps = 8;
 
 __global__ void tile_init_kernel(float *m, float *l, float *acc, int rows)
 {
+    allow_dependent_launch();
+    grid_dependency_wait();
     const long n = static_cast<long>(rows) * kHeadDim;
     for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) tile_update_kernel(const Tile
     const int kvh = blockIdx.x;
     const int b = blockIdx.y;
 
+    allow_dependent_launch();
+    grid_dependency_wait();
     WarpAttn<G> st;
     st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim, p.scale_log2);
     const long stride = static_cast<long>(p.Hkv) * kRowBytes; // one position, all KV heads
@@ -107,6 +111,8 @@ __global__ void __launch_bounds__(kTileWarps * 32) tile_update_kernel(const Tile
 __global__ void tile_finalize_kernel(const float *l, const float *acc, int rows, float *out_f32,
                                      uint16_t *out_bf16)
 {
+    allow_dependent_launch();
+    grid_dependency_wait();
     const long n = static_cast<long>(rows) * kHeadDim;
     for (long i = blockIdx.x * static_cast<long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -132,9 +138,8 @@ cudaError_t launch_tile_init(float *m, float *l, float *acc, int B, int Hq, cuda
     const int rows = B * Hq;
     if (rows == 0)
         return cudaSuccess;
-    tile_init_kernel<<<elementwise_blocks(static_cast<long>(rows) * kHeadDim), 256, 0, stream>>>(
-        m, l, acc, rows);
-    return cudaGetLastError();
+    return launch_pdl(tile_init_kernel, dim3(elementwise_blocks(static_cast<long>(rows) * kHeadDim)),
+                      dim3(256), 0, stream, m, l, acc, rows);
 }
 
 cudaError_t launch_tile_update(const TileArgs &a, cudaStream_t stream)
@@ -154,18 +159,18 @@ cudaError_t launch_tile_update(const TileArgs &a, cudaStream_t stream)
     p.acc = a.acc;
     const dim3 grid(a.Hkv, a.B);
     const int threads = kTileWarps * 32;
+    const dim3 block(threads);
     switch (a.Hq / a.Hkv) {
-    case 1: tile_update_kernel<1><<<grid, threads, 0, stream>>>(p); break;
-    case 2: tile_update_kernel<2><<<grid, threads, 0, stream>>>(p); break;
-    case 3: tile_update_kernel<3><<<grid, threads, 0, stream>>>(p); break;
-    case 4: tile_update_kernel<4><<<grid, threads, 0, stream>>>(p); break;
-    case 5: tile_update_kernel<5><<<grid, threads, 0, stream>>>(p); break;
-    case 6: tile_update_kernel<6><<<grid, threads, 0, stream>>>(p); break;
-    case 7: tile_update_kernel<7><<<grid, threads, 0, stream>>>(p); break;
-    case 8: tile_update_kernel<8><<<grid, threads, 0, stream>>>(p); break;
+    case 1: return launch_pdl(tile_update_kernel<1>, grid, block, 0, stream, p);
+    case 2: return launch_pdl(tile_update_kernel<2>, grid, block, 0, stream, p);
+    case 3: return launch_pdl(tile_update_kernel<3>, grid, block, 0, stream, p);
+    case 4: return launch_pdl(tile_update_kernel<4>, grid, block, 0, stream, p);
+    case 5: return launch_pdl(tile_update_kernel<5>, grid, block, 0, stream, p);
+    case 6: return launch_pdl(tile_update_kernel<6>, grid, block, 0, stream, p);
+    case 7: return launch_pdl(tile_update_kernel<7>, grid, block, 0, stream, p);
+    case 8: return launch_pdl(tile_update_kernel<8>, grid, block, 0, stream, p);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_tile_finalize(const float *m, const float *l, const float *acc, int B, int Hq,
@@ -175,9 +180,8 @@ cudaError_t launch_tile_finalize(const float *m, const float *l, const float *ac
     const int rows = B * Hq;
     if (rows == 0)
         return cudaSuccess;
-    tile_finalize_kernel<<<elementwise_blocks(static_cast<long>(rows) * kHeadDim), 256, 0, stream>>>(
-        l, acc, rows, out_f32, reinterpret_cast<uint16_t *>(out_bf16));
-    return cudaGetLastError();
+    return launch_pdl(tile_finalize_kernel, dim3(elementwise_blocks(static_cast<long>(rows) * kHeadDim)),
+                      dim3(256), 0, stream, l, acc, rows, out_f32, reinterpret_cast<uint16_t *>(out_bf16));
 }
 
 } // namespace pgqa

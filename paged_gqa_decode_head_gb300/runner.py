@@ -87,7 +87,7 @@ class DecodeStep:
             ws_bytes = max(ws_bytes, binding.decode_attn_workspace_size(
                 B, Hq, Hkv, self.D, kv.page_size, kv.max_pages, num_partitions))
         self.num_partitions = int(num_partitions)
-        self.workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=self.device)
+        self.workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=self.device)
         self.graph: torch.cuda.CUDAGraph | None = None
 
     @property

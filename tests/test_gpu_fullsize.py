@@ -51,7 +51,7 @@ def test_ragged_b64_full_size_sampled():
     qd = to_device_bf16(q, dev)
     kc, vc = to_device_bf16(kv.k_cache, dev), to_device_bf16(kv.v_cache, dev)
     bt, ctx = to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev)
-    ws = torch.empty(max(16, pg.decode_attn_workspace_size(B, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, 0)),
+    ws = torch.zeros(max(16, pg.decode_attn_workspace_size(B, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, 0)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((B, w["Hq"], 128), dtype=torch.float32, device=dev)
     pg.decode_attn_paged(qd, kc, vc, bt, ctx, SCALE, out_f32=out, workspace=ws)
@@ -75,7 +75,7 @@ def test_long_split_kv_t131072_np256():
     dev = "cuda"
     np_req = w["T"] // w["partition"]
     assert pg.decode_attn_partition_count(1, w["Hkv"], 16, kv.max_pages, np_req) == 256
-    ws = torch.empty(pg.decode_attn_workspace_size(1, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, np_req),
+    ws = torch.zeros(pg.decode_attn_workspace_size(1, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, np_req),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((1, w["Hq"], 128), dtype=torch.float32, device=dev)
     outb = torch.empty((1, w["Hq"], 128), dtype=torch.bfloat16, device=dev)

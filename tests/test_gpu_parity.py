@@ -41,7 +41,7 @@ def gpu_decode(q_bits, kv, scale=SCALE, num_partitions=0, out_f32=True, out_bf16
     B, Hq, D = q_bits.shape
     Hkv = kv.k_cache.shape[1]
     ws_bytes = pg.decode_attn_workspace_size(B, Hq, Hkv, D, kv.page_size, kv.max_pages, num_partitions)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     of = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=dev) if out_f32 else None
     ob = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev) if out_bf16 else None
     pg.decode_attn_paged(q, kc, vc, bt, ctx, scale, out_f32=of, out_bf16=ob, workspace=ws,
@@ -188,6 +188,36 @@ def test_decode_group_sizes(Hq, Hkv):
     q = inputs.query(70 + Hq, len(ctx), Hq)
     check_attention(q, kv, 0)
     check_attention(q, kv, 5)
+
+
+@pytest.mark.parametrize("num_partitions", [65, 94, 188])
+def test_decode_many_partitions_use_the_merge_kernel(num_partitions):
+    # more partitions than the split kernel merges in its last CTA
+    ctx = [3000, 1500, 40]
+    kv = inputs.paged_kv(86, ctx, Hkv=8, page_size=16)
+    q = inputs.query(86, len(ctx), 32)
+    check_attention(q, kv, num_partitions)
+
+
+def test_decode_repeated_calls_reuse_the_workspace():
+    # the partition tickets must come back to zero after every call
+    kv = inputs.paged_kv(87, [2000, 3001], Hkv=8, page_size=16)
+    q = inputs.query(87, 2, 16)
+    dev = "cuda"
+    args = (to_device_bf16(q, dev), to_device_bf16(kv.k_cache, dev), to_device_bf16(kv.v_cache, dev),
+            to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev), SCALE)
+    ws = torch.zeros(pg.decode_attn_workspace_size(2, 16, 8, 128, 16, kv.max_pages, 12), dtype=torch.uint8,
+                     device=dev)
+    outs = []
+    for _ in range(3):
+        out = torch.full((2, 16, 128), float("nan"), device=dev)
+        pg.decode_attn_paged(*args, out_f32=out, workspace=ws, num_partitions=12)
+        outs.append(out)
+    torch.cuda.synchronize()
+    ref = oracle.decode_attention(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, SCALE)
+    for out in outs:
+        assert np.abs(out.cpu().numpy() - ref).max() <= ATOL_F32
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
 def test_decode_ragged_batch_with_empty_sequence():

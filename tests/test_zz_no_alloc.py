@@ -36,7 +36,7 @@ def _case(seed, ctx, Hq=16, Hkv=8, P=16):
 
 
 def _with_workspace(c, np_):
-    ws = torch.empty(max(16, pg.decode_attn_workspace_size(c["B"], c["Hq"], c["Hkv"], 128, c["P"], c["max_pages"],
+    ws = torch.zeros(max(16, pg.decode_attn_workspace_size(c["B"], c["Hq"], c["Hkv"], 128, c["P"], c["max_pages"],
                                                            np_)), dtype=torch.uint8, device="cuda")
     of = torch.empty((c["B"], c["Hq"], 128), dtype=torch.float32, device="cuda")
     ob = torch.empty((c["B"], c["Hq"], 128), dtype=torch.bfloat16, device="cuda")

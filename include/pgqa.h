@@ -165,6 +165,31 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
                       size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * decode_step_paged -- one layer's whole decode step in one launch:
+ * qk_norm_rope_append (s2.3, s2.4, s7.2) followed by decode_attn_paged
+ * (s2.5, s2.6, s9.1, s10.1, s10.2), with the same results as calling the two
+ * in order. Each attention CTA normalises and rotates the query heads it
+ * serves; the CTA whose partition holds the new position appends the new
+ * token's K and V to the cache. Fusing removes a launch and a dependency from
+ * the per-layer chain, and lets every history chunk be requested before the
+ * previous kernel in the stream finishes.
+ *
+ *   q, k, v, gamma_q, gamma_k, context_lens (T_b >= 1), block_table,
+ *   k_cache, v_cache, rope_theta, eps     as for qk_norm_rope_append
+ *   q_out    [B][Hq][D] bf16, nullable: the rotated query, if wanted
+ *   scale, num_partitions, out_f32, out_bf16, workspace, ws_bytes
+ *                                        as for decode_attn_paged
+ * Sequences with T_b < 1 raise PGQA_DEVERR_BAD_CONTEXT and produce zeros.
+ */
+int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                      const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                      const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
+                      pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D,
+                      int page_size, int max_pages, int num_pages, float rope_theta, float eps,
+                      float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                      void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * attn_partition_merge -- exact merge of NP partition states (s9.1).
  *   m, l  [B][Hq][NP] float   running max of the scores (natural-log units)
  *                             and the softmax denominator, both relative to m

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     attn_tile_update,
     decode_attn_paged,
     decode_attn_paged_static,
+    decode_step_paged,
     decode_attn_partition_count,
     decode_attn_workspace_size,
     device_error_flags,

@@ -231,6 +231,78 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
     return ok();
 }
 
+int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                      const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                      const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
+                      pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D,
+                      int page_size, int max_pages, int num_pages, float rope_theta, float eps,
+                      float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                      void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "decode_step_paged";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (int st = check_pages(fn, page_size, max_pages, num_pages))
+        return st;
+    if (num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
+    if (!std::isfinite(scale))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: rope_theta must be > 0 and eps >= 0", fn);
+    if (static_cast<long long>(num_pages) * Hkv * page_size > 0x7FFFFFFFLL)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: num_pages * Hkv * page_size exceeds 2^31 - 1 rows", fn);
+    if (B == 0)
+        return ok();
+    if (!q || !k || !v || !gamma_q || !gamma_k || !context_lens || !block_table || !k_cache ||
+        !v_cache)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!out_f32 && !out_bf16)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: out_f32 and out_bf16 are both NULL", fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gamma_q) ||
+        !aligned16(gamma_k) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (q_out && !aligned16(q_out)) || (out_f32 && !aligned16(out_f32)) ||
+        (out_bf16 && !aligned16(out_bf16)) || !aligned4(context_lens) || !aligned4(block_table) ||
+        (workspace && !aligned16(workspace)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
+    const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                           sm_count_current_device());
+    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu",
+                    fn, need, np, workspace ? ws_bytes : static_cast<size_t>(0));
+    pgqa::DecodeArgs a{};
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.num_partitions = np;
+    a.pages_per_part = max_pages > 0 ? (max_pages + np - 1) / np : 1;
+    a.out_f32 = out_f32;
+    a.out_bf16 = out_bf16;
+    a.ws = static_cast<float *>(workspace);
+    a.fused = true;
+    a.q_raw = q;
+    a.k_new = k;
+    a.v_new = v;
+    a.gamma_q = gamma_q;
+    a.gamma_k = gamma_k;
+    a.q_out = q_out;
+    a.rope_theta = static_cast<double>(rope_theta);
+    a.eps = eps;
+    cudaError_t err = pgqa::launch_decode(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
 int attn_partition_merge(const float *m, const float *l, const float *acc, int B, int Hq, int D,
                          int NP, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t stream)
 {

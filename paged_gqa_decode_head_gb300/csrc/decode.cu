@@ -15,8 +15,8 @@
 // * Grid = (partition, KV head, sequence), one 288-thread CTA per SM. Each of
 //   the 9 warps owns every 9th 16-position chunk of the partition and a
 //   private ring of 3 shared-memory stages (27 chunks = 216 KiB per CTA). Lane
-//   0 issues four 2-D TMA loads per chunk (K and V, dims 0-63 and 64-127, 16
-//   rows each, 128-byte swizzle) that complete on the stage's mbarrier.
+//   0 issues one 3-D TMA load per 4 KiB chunk of K and of V (16 rows, two
+//   64-column halves, 128-byte swizzle) that complete on the stage's mbarrier.
 // * The warp folds its resident chunks together with tensor-core MMAs
 //   (mma.sync m16n8k16, bf16 in, fp32 accumulate), transposed so the g <= 8
 //   query heads fill the N = 8 columns: S^T = K Q^T, the online softmax on the
@@ -42,6 +42,7 @@
 #include <cuda.h>
 
 #include "attn_core.cuh"
+#include "head_norm_rope.cuh"
 #include "launch.h"
 
 namespace pgqa {
@@ -59,9 +60,10 @@ constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-by
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
-constexpr int kSplitSmem = 1024 /* alignment slack */ + kWarps * kStages * kStageBytes +
-                           kWarps * kStages * 8 /* mbarriers */ +
-                           kWarps * kStages * 4 /* valid rows per stage */ + 16 /* ticket */;
+constexpr int kQBufOffset = kWarps * kStages * kStageBytes + kWarps * kStages * 8 /* mbarriers */ +
+                            kWarps * kStages * 4 /* valid rows per stage */ + 16 /* ticket */;
+constexpr int kSplitSmem = 1024 /* alignment slack */ + kQBufOffset +
+                           kMaxGroup * kHeadDim * 2 /* rotated q of the fused step */;
 
 struct SplitParams {
     const uint16_t *q;
@@ -73,6 +75,12 @@ struct SplitParams {
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
     int fused_merge;
     float scale_log2;
+    // fused decode step only: the new token's raw heads and the prologue's
+    // parameters; the kernel normalises/rotates q and appends K/V itself
+    const uint16_t *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
+    uint16_t *k_cache, *v_cache, *q_out;
+    float eps;
+    double inv_freq[kHeadDim / 2];
 };
 
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p)
@@ -339,7 +347,12 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, f
     }
 }
 
-template <int G>
+// kFused = true: the whole decode step of one layer (qk_norm_rope_append
+// then decode attention) in one launch. Each CTA normalises and rotates the
+// query heads it serves; the warp whose chunk holds position T-1 computes the
+// new K row, appends K and V to the cache and patches the row into its staged
+// chunk, so every history chunk can be requested before griddepcontrol.wait.
+template <int G, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const SplitParams p)
@@ -354,6 +367,19 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     const int b = blockIdx.z;
 
     allow_dependent_launch();
+    unsigned char *stages = smem + warp * kStages * kStageBytes;
+    uint64_t *bars =
+        reinterpret_cast<uint64_t *>(smem + kWarps * kStages * kStageBytes) + warp * kStages;
+    if (lane == 0) {
+        if (warp == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
 
     const int part_tokens = p.ppp * p.P;
     const int tok0 = part * part_tokens;
@@ -369,7 +395,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         tbl_val = (chunk_token(lane) < tok0 + part_tokens && page < p.max_pages) ? table[page] : -1;
     }
     int T = p.context_lens[b];
-    if (T < 0 || T > p.max_pages * p.P) {
+    if (T < (kFused ? 1 : 0) || T > p.max_pages * p.P) {
         if (part == 0 && threadIdx.x == 0)
             raise_flag(PGQA_DEVERR_BAD_CONTEXT);
         T = 0;
@@ -383,23 +409,17 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     const int n_chunks = max(0, (tok1 - tok0 + kChunkTokens - 1) / kChunkTokens);
     const int my_chunks = (n_chunks > warp) ? (n_chunks - 1 - warp) / kWarps + 1 : 0;
 
-    unsigned char *stages = smem + warp * kStages * kStageBytes;
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + kWarps * kStages * kStageBytes) + warp * kStages;
     int *stage_rows =
         reinterpret_cast<int *>(smem + kWarps * kStages * kStageBytes + kWarps * kStages * 8) +
         warp * kStages;
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < kStages; ++s)
-            mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
     __syncwarp();
 
     // The chunk holding position T-1 is written by the prologue this kernel
-    // may overlap, so it is requested only after griddepcontrol.wait.
-    auto holds_new_token = [&](int k) { return chunk_token(k) + kChunkTokens > T - 1; };
+    // may overlap, so it is requested only after griddepcontrol.wait (the
+    // fused step patches that row into shared memory itself instead).
+    auto holds_new_token = [&](int k) {
+        return !kFused && chunk_token(k) + kChunkTokens > T - 1;
+    };
     // Physical pages of this warp's chunks, 32 at a time: lane L caches the
     // entry of chunk 32*blk + L. Called by the whole (converged) warp.
     auto phys_of = [&](int k) {
@@ -424,10 +444,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         const int row = (phys * p.Hkv + kvh) * p.P + (t % p.P);
         unsigned char *dst = stages + (k % kStages) * kStageBytes;
         mbar_arrive_expect_tx(bar, kStageBytes);
-        tma_load_2d(dst, &tmap_k, 0, row, bar, policy);
-        tma_load_2d(dst + kBoxBytes, &tmap_k, 64, row, bar, policy);
-        tma_load_2d(dst + 2 * kBoxBytes, &tmap_v, 0, row, bar, policy);
-        tma_load_2d(dst + 3 * kBoxBytes, &tmap_v, 64, row, bar, policy);
+        tma_load_3d(dst, &tmap_k, 0, row, 0, bar, policy);
+        tma_load_3d(dst + 2 * kBoxBytes, &tmap_v, 0, row, 0, bar, policy);
     };
 
     const uint64_t policy = l2_evict_first_policy();
@@ -452,7 +470,55 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncwarp();
 
     MmaWarp<G> st;
-    st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
+    // fused step: the new token's K/V row, kept by the warp owning its chunk
+    uint16_t new_k[4] = {0, 0, 0, 0}, new_v[4] = {0, 0, 0, 0};
+    int new_chunk = -1; // index k of that chunk in this warp's sequence, or -1
+    if constexpr (kFused) {
+        uint16_t *q_buf = reinterpret_cast<uint16_t *>(smem + kQBufOffset);
+        const int pos = T - 1;
+        if (T > 0 && warp < G) {
+            const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * G + warp) * kHeadDim;
+            float x[4];
+            norm_rope_head(p.q_raw + qrow, p.gamma_q, p.eps, pos, p.inv_freq, x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint16_t bits = f32_to_bf16_bits(x[i]);
+                q_buf[warp * kHeadDim + lane + 32 * i] = bits;
+                if (part == 0 && p.q_out)
+                    p.q_out[qrow + lane + 32 * i] = bits;
+            }
+        }
+        if (T > 0 && pos >= tok0 && pos < tok1) {
+            const int c_idx = (pos - tok0) / kChunkTokens;
+            if (c_idx % kWarps == warp) {
+                new_chunk = c_idx / kWarps;
+                const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
+                float x[4];
+                norm_rope_head(p.k_new + krow, p.gamma_k, p.eps, pos, p.inv_freq, x);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    new_k[i] = f32_to_bf16_bits(x[i]);
+                    new_v[i] = p.v_new[krow + lane + 32 * i];
+                }
+                const int phys = table[pos / p.P];
+                if (phys >= 0 && phys < p.num_pages) {
+                    const size_t slot =
+                        ((static_cast<size_t>(phys) * p.Hkv + kvh) * p.P + pos % p.P) * kHeadDim;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        p.k_cache[slot + lane + 32 * i] = new_k[i];
+                        p.v_cache[slot + lane + 32 * i] = new_v[i];
+                    }
+                } else if (lane == 0) {
+                    raise_flag(PGQA_DEVERR_BAD_PAGE);
+                }
+            }
+        }
+        __syncthreads();
+        st.init(q_buf);
+    } else {
+        st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
+    }
 
     // Chunks are consumed in groups of up to kStages (one per stage); the
     // group's stages are refilled together once it has been folded.
@@ -472,6 +538,20 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                 if (!__all_sync(0xFFFFFFFFu, landed))
                     ok = false;
                 rows[c] = stage_rows[k % kStages];
+                if (kFused && k == new_chunk && rows[c] > 0) {
+                    // the staged copy predates the append: put the new row in
+                    const int r = (T - 1) % kChunkTokens;
+                    unsigned char *stage = stages + (k % kStages) * kStageBytes;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int d = lane + 32 * i;
+                        const int x = d & 63, u = x >> 3;
+                        const int off = (d >> 6) * kBoxBytes + r * 128 + ((u ^ (r & 7)) << 4) + (x & 7) * 2;
+                        *reinterpret_cast<uint16_t *>(stage + off) = new_k[i];
+                        *reinterpret_cast<uint16_t *>(stage + 2 * kBoxBytes + off) = new_v[i];
+                    }
+                    __syncwarp();
+                }
                 if (rows[c] < kChunkTokens) {
                     // Rows past the history (all rows of a chunk whose page
                     // was refused) may hold anything, even NaN: zero their V
@@ -707,26 +787,30 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D map over a paged cache seen as [num_pages * Hkv * P rows][128 bf16]:
-// boxes of 16 rows x 64 columns, 128-byte swizzle.
+// A paged cache seen as a 3-D tensor [2 halves][num_pages * Hkv * P rows]
+// [64 bf16]: element (x, row, half) is column 64*half + x of that row. One
+// box {64, 16, 2} is a whole 16-row chunk, landing in shared memory as the
+// 16 rows of columns 0-63 followed by the 16 rows of columns 64-127, each
+// 128-byte line swizzled (128-byte swizzle), so ldmatrix reads it without
+// bank conflicts; one TMA instruction moves a 4 KiB chunk of K (or V).
 cudaError_t encode_cache_map(CUtensorMap *map, const void *base, long long rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRowBytes)};
-    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kChunkTokens)};
-    const cuuint32_t elem[2] = {1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+    const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), 2u};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRowBytes), 128u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kChunkTokens), 2u};
+    const cuuint32_t elem[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G>
-cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
-                         dim3 grid, cudaStream_t stream)
+template <int G, bool kFused>
+cudaError_t launch_split_t(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
+                           dim3 grid, cudaStream_t stream)
 {
     static bool configured[kMaxDevices] = {};
     int dev = 0;
@@ -734,14 +818,23 @@ cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const Spl
     if (err != cudaSuccess)
         return err;
     if (dev >= kMaxDevices || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSplitSmem);
+        err = cudaFuncSetAttribute(decode_mma_kernel<G, kFused>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < kMaxDevices)
             configured[dev] = true;
     }
-    return launch_pdl(decode_mma_kernel<G>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk, mv, kp);
+    return launch_pdl(decode_mma_kernel<G, kFused>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk,
+                      mv, kp);
+}
+
+template <int G>
+cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
+                         dim3 grid, bool fused, cudaStream_t stream)
+{
+    return fused ? launch_split_t<G, true>(mk, mv, kp, grid, stream)
+                 : launch_split_t<G, false>(mk, mv, kp, grid, stream);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -816,6 +909,19 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
     kp.fused_merge = a.num_partitions <= kFusedMergeMax ? 1 : 0;
+    if (a.fused) {
+        kp.q_raw = a.q_raw;
+        kp.k_new = a.k_new;
+        kp.v_new = a.v_new;
+        kp.gamma_q = a.gamma_q;
+        kp.gamma_k = a.gamma_k;
+        kp.k_cache = const_cast<uint16_t *>(a.k_cache);
+        kp.v_cache = const_cast<uint16_t *>(a.v_cache);
+        kp.q_out = a.q_out;
+        kp.eps = a.eps;
+        for (int i = 0; i < kHeadDim / 2; ++i)
+            kp.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / kHeadDim);
+    }
     if (a.num_partitions > 1) {
         const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;
         char *ws = reinterpret_cast<char *>(a.ws);
@@ -827,14 +933,14 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
     switch (G) {
-    case 1: err = launch_split<1>(mk, mv, kp, grid, stream); break;
-    case 2: err = launch_split<2>(mk, mv, kp, grid, stream); break;
-    case 3: err = launch_split<3>(mk, mv, kp, grid, stream); break;
-    case 4: err = launch_split<4>(mk, mv, kp, grid, stream); break;
-    case 5: err = launch_split<5>(mk, mv, kp, grid, stream); break;
-    case 6: err = launch_split<6>(mk, mv, kp, grid, stream); break;
-    case 7: err = launch_split<7>(mk, mv, kp, grid, stream); break;
-    case 8: err = launch_split<8>(mk, mv, kp, grid, stream); break;
+    case 1: err = launch_split<1>(mk, mv, kp, grid, a.fused, stream); break;
+    case 2: err = launch_split<2>(mk, mv, kp, grid, a.fused, stream); break;
+    case 3: err = launch_split<3>(mk, mv, kp, grid, a.fused, stream); break;
+    case 4: err = launch_split<4>(mk, mv, kp, grid, a.fused, stream); break;
+    case 5: err = launch_split<5>(mk, mv, kp, grid, a.fused, stream); break;
+    case 6: err = launch_split<6>(mk, mv, kp, grid, a.fused, stream); break;
+    case 7: err = launch_split<7>(mk, mv, kp, grid, a.fused, stream); break;
+    case 8: err = launch_split<8>(mk, mv, kp, grid, a.fused, stream); break;
     default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)

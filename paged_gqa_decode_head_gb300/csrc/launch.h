@@ -31,6 +31,12 @@ struct DecodeArgs {
     float *out_f32;      // nullable
     pgqa_bf16 *out_bf16; // nullable
     float *ws;           // partial states when NP > 1
+    // fused decode step (qk_norm_rope_append + attention in one launch)
+    bool fused;
+    const pgqa_bf16 *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
+    pgqa_bf16 *q_out; // nullable
+    double rope_theta;
+    float eps;
 };
 
 struct MergeArgs {

@@ -11,11 +11,10 @@
 //   s7.2 the rotated K goes straight to its physical page
 //        block_table[b][pos / P] at offset pos % P.
 //
-// The RoPE phase pos * omega_i is formed in fp64 (omega_i is computed on the
-// host in fp64) and reduced modulo 2*pi before the fp32 sincosf, so the angle
-// stays accurate to ~1e-7 rad even at pos ~ 1e5 where an fp32 product would
-// be off by ~1e-2 rad.
+// The norm and rotation of one head are in head_norm_rope.cuh (shared with
+// the fused decode step).
 #include "common.cuh"
+#include "head_norm_rope.cuh"
 #include "launch.h"
 
 namespace pgqa {
@@ -34,30 +33,6 @@ struct PrologueParams {
     float eps;
     double inv_freq[kHalf]; // theta^(-2i/D), i < D/2
 };
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
-{
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
-}
-
-// Rotate the pair (a, b) of frequency index i at position pos.
-__device__ __forceinline__ void rope_pair(float &a, float &b, int pos, double inv_freq)
-{
-    // 2*pi as an unevaluated sum hi + lo of two doubles.
-    constexpr double kTwoPiHi = 6.283185307179586232;
-    constexpr double kTwoPiLo = 2.4492935982947064e-16;
-    constexpr double kInvTwoPi = 0.15915494309189535;
-    const double phi = static_cast<double>(pos) * inv_freq;
-    const double n = rint(phi * kInvTwoPi);
-    double r = fma(-n, kTwoPiHi, phi);
-    r = fma(-n, kTwoPiLo, r);
-    float sn, cs;
-    sincosf(static_cast<float>(r), &sn, &cs);
-    const float ra = a * cs - b * sn;
-    const float rb = b * cs + a * sn;
-    a = ra;
-    b = rb;
-}
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
 {
@@ -106,20 +81,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
     }
 
     float x[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        x[i] = bf16_bits_to_f32(src[lane + 32 * i]);
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    const float inv_rms = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        x[i] = x[i] * inv_rms * bf16_bits_to_f32(gamma[lane + 32 * i]);
-    // pairs (lane, lane + 64) and (lane + 32, lane + 96)
-    rope_pair(x[0], x[2], pos, p.inv_freq[lane]);
-    rope_pair(x[1], x[3], pos, p.inv_freq[lane + 32]);
+    norm_rope_head(src, gamma, p.eps, pos, p.inv_freq, x);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         dst[lane + 32 * i] = f32_to_bf16_bits(x[i]);

@@ -96,8 +96,14 @@ class DecodeStep:
         return binding.decode_attn_partition_count(st.block_table.shape[0], self.Hkv, st.page_size,
                                                    st.block_table.shape[1], self.num_partitions)
 
-    def run_layer(self, i: int, stream=None, prologue: bool = True) -> None:
+    def run_layer(self, i: int, stream=None, prologue: bool = True, fused: bool = False) -> None:
         st = self.layers[i]
+        if prologue and fused:
+            binding.decode_step_paged(st.q, st.k, st.v, st.gamma_q, st.gamma_k, st.context_lens, st.block_table,
+                                      st.k_cache, st.v_cache, self.scale, self.rope_theta, self.eps, q_out=st.q_out,
+                                      out_f32=st.out_f32, out_bf16=st.out_bf16, workspace=self.workspace,
+                                      num_partitions=self.num_partitions, stream=stream)
+            return
         if prologue:
             binding.qk_norm_rope_append(st.q, st.k, st.v, st.gamma_q, st.gamma_k, st.context_lens, st.block_table,
                                         st.k_cache, st.v_cache, st.q_out, st.page_size, self.rope_theta, self.eps,
@@ -106,20 +112,22 @@ class DecodeStep:
                                   out_f32=st.out_f32, out_bf16=st.out_bf16, workspace=self.workspace,
                                   num_partitions=self.num_partitions, stream=stream)
 
-    def run(self, stream=None, prologue: bool = True) -> None:
+    def run(self, stream=None, prologue: bool = True, fused: bool = False) -> None:
+        """One step: per layer the prologue and the attention, as two launches
+        or (fused=True) as one decode_step_paged launch."""
         for i in range(len(self.layers)):
-            self.run_layer(i, stream=stream, prologue=prologue)
+            self.run_layer(i, stream=stream, prologue=prologue, fused=fused)
 
-    def capture(self, prologue: bool = True) -> torch.cuda.CUDAGraph:
+    def capture(self, prologue: bool = True, fused: bool = False) -> torch.cuda.CUDAGraph:
         """Record one whole step (every layer) into a CUDA graph."""
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
-            self.run(prologue=prologue)  # warm-up outside capture
+            self.run(prologue=prologue, fused=fused)  # warm-up outside capture
         torch.cuda.current_stream(self.device).wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(prologue=prologue)
+            self.run(prologue=prologue, fused=fused)
         self.graph = g
         return g
 

@@ -20,11 +20,14 @@ ATOL_F32 = 2e-3
 SCALE = 1.0 / math.sqrt(128)
 
 
-def test_qwen3_28_layer_step_t8192_graph():
+@pytest.mark.parametrize("fused", [True, False])
+def test_qwen3_28_layer_step_t8192_graph(fused):
+    """The benchmark's step (fused: one decode_step_paged launch per layer;
+    otherwise qk_norm_rope_append + decode_attn_paged) replayed as one graph."""
     w = inputs.WORKLOADS["qwen3_0p6b_t8k"]
     layers = inputs.qwen3_layers()
     step = DecodeStep(layers, Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"])
-    step.capture()
+    step.capture(fused=fused)
     step.replay()
     torch.cuda.synchronize()
     assert pg.device_error_flags() == 0

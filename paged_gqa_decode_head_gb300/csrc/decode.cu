@@ -60,6 +60,7 @@ constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-by
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
+constexpr int kPrewaitChunks = 1;               // chunks per warp requested before the grid wait
 constexpr int kQBufOffset = kWarps * kStages * kStageBytes + kWarps * kStages * 8 /* mbarriers */ +
                             kWarps * kStages * 4 /* valid rows per stage */ + 16 /* ticket */;
 constexpr int kSplitSmem = 1024 /* alignment slack */ + kQBufOffset +
@@ -454,70 +455,100 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
+    // Only the first kPrewaitChunks chunks of each warp are requested before
+    // griddepcontrol.wait: the rest would queue in the memory system ahead of
+    // the previous layer's merge and this layer's query loads, which sit on
+    // the critical path of the layer chain.
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && !holds_new_token(k))
+            if (k < first && k < kPrewaitChunks && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
+
+    // fused step: what the prologue needs that no earlier kernel writes
+    // (gains, rotation, the append slot) is prepared before the wait.
+    const int pos = T - 1;
+    const bool has_q = kFused && T > 0 && warp < G;
+    int new_chunk = -1; // index k of the chunk holding pos in this warp's sequence, or -1
+    int new_phys = -1;
+    if (kFused && T > 0 && pos >= tok0 && pos < tok1) {
+        const int c_idx = (pos - tok0) / kChunkTokens;
+        if (c_idx % kWarps == warp) {
+            new_chunk = c_idx / kWarps;
+            new_phys = table[pos / p.P];
+        }
+    }
+    HeadRope rope;
+    float gain_q[4], gain_k[4];
+    if (has_q || new_chunk >= 0)
+        rope.init(pos, p.inv_freq);
+    if (has_q)
+        load_head(p.gamma_q, gain_q);
+    if (new_chunk >= 0)
+        load_head(p.gamma_k, gain_k);
+
     grid_dependency_wait();
+
+    // The new token's q, k, v come from the previous kernels: load them now,
+    // ahead of the remaining bulk requests.
+    const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * G + warp) * kHeadDim;
+    const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
+    float xq[4], xk[4];
+    uint16_t new_v[4] = {0, 0, 0, 0};
+    MmaWarp<G> st;
+    if (has_q)
+        load_head(p.q_raw + qrow, xq);
+    if (new_chunk >= 0) {
+        load_head(p.k_new + krow, xk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            new_v[i] = p.v_new[krow + lane + 32 * i];
+    }
+    if constexpr (!kFused)
+        st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && holds_new_token(k))
+            if (k < first && (k >= kPrewaitChunks || holds_new_token(k)))
                 issue(k, first_phys[k], policy);
     }
     __syncwarp();
 
-    MmaWarp<G> st;
-    // fused step: the new token's K/V row, kept by the warp owning its chunk
-    uint16_t new_k[4] = {0, 0, 0, 0}, new_v[4] = {0, 0, 0, 0};
-    int new_chunk = -1; // index k of that chunk in this warp's sequence, or -1
+    // fused step: normalise and rotate q (warps < G) and the new K row (the
+    // warp owning its chunk), append K and V to the cache.
+    uint16_t new_k[4] = {0, 0, 0, 0};
     if constexpr (kFused) {
         uint16_t *q_buf = reinterpret_cast<uint16_t *>(smem + kQBufOffset);
-        const int pos = T - 1;
-        if (T > 0 && warp < G) {
-            const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * G + warp) * kHeadDim;
-            float x[4];
-            norm_rope_head(p.q_raw + qrow, p.gamma_q, p.eps, pos, p.inv_freq, x);
+        if (has_q) {
+            norm_rope_apply(xq, gain_q, p.eps, rope);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint16_t bits = f32_to_bf16_bits(x[i]);
+                const uint16_t bits = f32_to_bf16_bits(xq[i]);
                 q_buf[warp * kHeadDim + lane + 32 * i] = bits;
                 if (part == 0 && p.q_out)
                     p.q_out[qrow + lane + 32 * i] = bits;
             }
         }
-        if (T > 0 && pos >= tok0 && pos < tok1) {
-            const int c_idx = (pos - tok0) / kChunkTokens;
-            if (c_idx % kWarps == warp) {
-                new_chunk = c_idx / kWarps;
-                const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
-                float x[4];
-                norm_rope_head(p.k_new + krow, p.gamma_k, p.eps, pos, p.inv_freq, x);
+        if (new_chunk >= 0) {
+            norm_rope_apply(xk, gain_k, p.eps, rope);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                new_k[i] = f32_to_bf16_bits(xk[i]);
+            if (new_phys >= 0 && new_phys < p.num_pages) {
+                const size_t slot =
+                    ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + pos % p.P) * kHeadDim;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    new_k[i] = f32_to_bf16_bits(x[i]);
-                    new_v[i] = p.v_new[krow + lane + 32 * i];
+                    p.k_cache[slot + lane + 32 * i] = new_k[i];
+                    p.v_cache[slot + lane + 32 * i] = new_v[i];
                 }
-                const int phys = table[pos / p.P];
-                if (phys >= 0 && phys < p.num_pages) {
-                    const size_t slot =
-                        ((static_cast<size_t>(phys) * p.Hkv + kvh) * p.P + pos % p.P) * kHeadDim;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        p.k_cache[slot + lane + 32 * i] = new_k[i];
-                        p.v_cache[slot + lane + 32 * i] = new_v[i];
-                    }
-                } else if (lane == 0) {
-                    raise_flag(PGQA_DEVERR_BAD_PAGE);
-                }
+            } else if (lane == 0) {
+                raise_flag(PGQA_DEVERR_BAD_PAGE);
             }
         }
         __syncthreads();
         st.init(q_buf);
-    } else {
-        st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
     }
 
     // Chunks are consumed in groups of up to kStages (one per stage); the

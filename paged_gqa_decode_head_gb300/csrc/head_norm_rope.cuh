@@ -20,8 +20,9 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h)
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
 }
 
-// Rotate the pair (a, b) whose frequency is inv_freq at position pos.
-__device__ __forceinline__ void rope_pair(float &a, float &b, int pos, double inv_freq)
+// cos and sin of the RoPE angle pos * inv_freq, the angle reduced modulo
+// 2*pi in fp64 first.
+__device__ __forceinline__ void rope_angle(int pos, double inv_freq, float &cs, float &sn)
 {
     // 2*pi as an unevaluated sum hi + lo of two doubles.
     constexpr double kTwoPiHi = 6.283185307179586232;
@@ -31,34 +32,65 @@ __device__ __forceinline__ void rope_pair(float &a, float &b, int pos, double in
     const double n = rint(phi * kInvTwoPi);
     double r = fma(-n, kTwoPiHi, phi);
     r = fma(-n, kTwoPiLo, r);
-    float sn, cs;
     sincosf(static_cast<float>(r), &sn, &cs);
-    const float ra = a * cs - b * sn;
-    const float rb = b * cs + a * sn;
-    a = ra;
-    b = rb;
 }
 
-// x[i] (dim lane + 32 i) of RoPE_pos(RMSNorm(src) * gamma); whole warp.
-// inv_freq[i] = theta^(-2i/128) for i < 64.
-__device__ __forceinline__ void norm_rope_head(const uint16_t *src, const uint16_t *gamma, float eps,
-                                               int pos, const double *inv_freq, float (&x)[4])
+// The rotation of this lane's two pairs (lane, lane + 64) and
+// (lane + 32, lane + 96) at position pos; inv_freq[i] = theta^(-2i/128).
+struct HeadRope {
+    float cs[2], sn[2];
+    __device__ __forceinline__ void init(int pos, const double *inv_freq)
+    {
+        const int lane = threadIdx.x & 31;
+        rope_angle(pos, inv_freq[lane], cs[0], sn[0]);
+        rope_angle(pos, inv_freq[lane + 32], cs[1], sn[1]);
+    }
+};
+
+// This lane's four elements (dims lane + 32 i) of a bf16 head vector.
+__device__ __forceinline__ void load_head(const uint16_t *src, float (&x)[4])
 {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         x[i] = bf16_bits_to_f32(src[lane + 32 * i]);
-    float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+}
+
+// x <- RoPE(RMSNorm(x) * gain) for the head held by the warp (x[i] is dim
+// lane + 32 i). Every product and sum is rounded explicitly (no contraction
+// left to the compiler), so every kernel that uses this gets the same bits.
+__device__ __forceinline__ void norm_rope_apply(float (&x)[4], const float (&gain)[4], float eps,
+                                                const HeadRope &rope)
+{
+    float ss = __fmul_rn(x[0], x[0]);
+    ss = __fmaf_rn(x[1], x[1], ss);
+    ss = __fmaf_rn(x[2], x[2], ss);
+    ss = __fmaf_rn(x[3], x[3], ss);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    const float inv_rms = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+        ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, off));
+    const float inv_rms = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), eps));
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-        x[i] = x[i] * inv_rms * bf16_bits_to_f32(gamma[lane + 32 * i]);
-    // pairs (lane, lane + 64) and (lane + 32, lane + 96)
-    rope_pair(x[0], x[2], pos, inv_freq[lane]);
-    rope_pair(x[1], x[3], pos, inv_freq[lane + 32]);
+        x[i] = __fmul_rn(__fmul_rn(x[i], inv_rms), gain[i]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float a = x[j], b = x[j + 2];
+        x[j] = __fmaf_rn(a, rope.cs[j], -__fmul_rn(b, rope.sn[j]));
+        x[j + 2] = __fmaf_rn(b, rope.cs[j], __fmul_rn(a, rope.sn[j]));
+    }
+}
+
+// x[i] (dim lane + 32 i) of RoPE_pos(RMSNorm(src) * gamma); whole warp.
+__device__ __forceinline__ void norm_rope_head(const uint16_t *src, const uint16_t *gamma, float eps,
+                                               int pos, const double *inv_freq, float (&x)[4])
+{
+    HeadRope rope;
+    rope.init(pos, inv_freq);
+    float gain[4];
+    load_head(gamma, gain);
+    load_head(src, x);
+    norm_rope_apply(x, gain, eps, rope);
 }
 
 } // namespace pgqa

@@ -60,11 +60,23 @@ constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-by
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
-constexpr int kPrewaitChunks = 1;               // chunks per warp requested before the grid wait
-constexpr int kQBufOffset = kWarps * kStages * kStageBytes + kWarps * kStages * 8 /* mbarriers */ +
-                            kWarps * kStages * 4 /* valid rows per stage */ + 16 /* ticket */;
-constexpr int kSplitSmem = 1024 /* alignment slack */ + kQBufOffset +
-                           kMaxGroup * kHeadDim * 2 /* rotated q of the fused step */;
+// Chunks per warp requested before the grid wait (measured on the 28-layer
+// T = 8192 chain): the fused step does best with 1, attention alone with all.
+template <bool kFused> constexpr int kPrewaitChunks = kFused ? 1 : kStages;
+// Shared memory (from a 1024-byte aligned base): the stages, one mbarrier and
+// one valid-row count per stage, the partition ticket, the merge's mbarrier,
+// the rotated query of the fused step.
+constexpr int kStageAreaBytes = kWarps * kStages * kStageBytes;
+constexpr int kBarOffset = kStageAreaBytes;
+constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
+constexpr int kTicketOffset = (kRowsOffset + kWarps * kStages * 4 + 7) & ~7;
+constexpr int kMergeBarOffset = kTicketOffset + 8;
+constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
+constexpr int kSplitSmem = 1024 /* alignment slack */ + kQBufOffset + kMaxGroup * kHeadDim * 2;
+// The in-kernel merge copies the G x n partition accumulators of its group
+// into the stage area, followed by its scratch (weights, sums, a float4 per
+// thread); launch_decode falls back to merge_kernel when they do not fit.
+constexpr int kMergeScratchBytes = kMaxGroup * kFusedMergeMax * 4 + 64 + kWarps * 32 * 16;
 
 struct SplitParams {
     const uint16_t *q;
@@ -81,7 +93,7 @@ struct SplitParams {
     const uint16_t *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
     uint16_t *k_cache, *v_cache, *q_out;
     float eps;
-    double inv_freq[kHeadDim / 2];
+    RopeFreqs freqs;
 };
 
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p)
@@ -261,17 +273,35 @@ template <int G> struct MmaWarp {
 
 // The last CTA of a (sequence, KV head) to finish merges the n (2..64)
 // partition states of its G query heads from the workspace (base-2 m) and
-// writes the outputs: one warp per head reduces M and L with shuffles, then
-// every thread folds its share of the acc rows, 8 independent loads at a time.
+// writes the outputs, in one round trip to memory: thread 0 copies the G x n
+// accumulators into shared memory (one bulk copy per head) while one warp per
+// head loads m and l and forms the weights e^(m_p - M) and L with shuffles;
+// then every thread folds its share of the accumulators from shared memory.
 template <int G>
-__device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, float *scratch)
+__device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, unsigned char *smem,
+                                  uint64_t *bar)
 {
     constexpr int kThreads = kWarps * 32;
-    float *w = scratch;                 // [G][kFusedMergeMax] weights e^(m_p - M)
-    float *Ls = w + G * kFusedMergeMax; // [G], padded to 16 floats
-    float *red = Ls + 16;               // [kThreads] float4 partial sums
+    float *acc = reinterpret_cast<float *>(smem);         // [G][n][128]
+    float *w = acc + static_cast<size_t>(G) * n * kHeadDim; // [G][kFusedMergeMax] weights
+    float *Ls = w + G * kFusedMergeMax;                     // [G], padded to 16 floats
+    float4 *red = reinterpret_cast<float4 *>(Ls + 16);      // [kThreads] partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        // the stage area was last used through the generic proxy, and the
+        // other CTAs' partition states were acquired through it
+        fence_proxy_async_smem();
+        fence_proxy_async_global();
+        const uint32_t row_bytes = static_cast<uint32_t>(n) * kHeadDim * 4;
+        mbar_arrive_expect_tx(bar, G * row_bytes);
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            bulk_copy_g2s_nohint(acc + static_cast<size_t>(h) * n * kHeadDim,
+                                 p.ws_acc + (row0 + h) * p.NP * kHeadDim, row_bytes, bar);
+    }
     for (int h = warp; h < G; h += kWarps) {
         const float *mh = p.ws_m + (row0 + h) * p.NP;
         const float *lh = p.ws_l + (row0 + h) * p.NP;
@@ -294,43 +324,38 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, f
             Ls[h] = L;
     }
     __syncthreads();
+    if (!mbar_wait_bounded(bar, 0)) {
+        // The copy never completed: flag it, give it one more bounded wait
+        // (it writes this CTA's shared memory) and leave the outputs alone.
+        if (threadIdx.x == 0)
+            raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
+        (void)mbar_wait_bounded(bar, 0);
+        return;
+    }
     constexpr int kItems = G * 32; // (head, 4 dims)
     constexpr int kSlices = kThreads >= kItems ? kThreads / kItems : 1;
     constexpr int kLanesPerSlice = kThreads / kSlices;
-    constexpr int kRound = 8;
     for (int base = 0; base < kItems; base += kLanesPerSlice) {
         const int item = base + (threadIdx.x % kLanesPerSlice);
         const int slice = threadIdx.x / kLanesPerSlice;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
         if (item < kItems && slice < kSlices) {
             const int h = item / 32, d4 = item % 32;
-            const float4 *src =
-                reinterpret_cast<const float4 *>(p.ws_acc + (row0 + h) * p.NP * kHeadDim) + d4;
-            for (int i0 = slice; i0 < n; i0 += kRound * kSlices) {
-                float4 v[kRound];
-#pragma unroll
-                for (int i = 0; i < kRound; ++i) {
-                    const int part = i0 + i * kSlices;
-                    v[i] = part < n ? __ldcg(src + static_cast<size_t>(part) * (kHeadDim / 4))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int i = 0; i < kRound; ++i) {
-                    const int part = i0 + i * kSlices;
-                    const float wt = part < n ? w[h * kFusedMergeMax + part] : 0.f;
-                    acc.x = fmaf(v[i].x, wt, acc.x);
-                    acc.y = fmaf(v[i].y, wt, acc.y);
-                    acc.z = fmaf(v[i].z, wt, acc.z);
-                    acc.w = fmaf(v[i].w, wt, acc.w);
-                }
+            const float4 *src = reinterpret_cast<const float4 *>(acc + static_cast<size_t>(h) * n * kHeadDim) + d4;
+            for (int part = slice; part < n; part += kSlices) {
+                const float4 v = src[static_cast<size_t>(part) * (kHeadDim / 4)];
+                const float wt = w[h * kFusedMergeMax + part];
+                sum.x = fmaf(v.x, wt, sum.x);
+                sum.y = fmaf(v.y, wt, sum.y);
+                sum.z = fmaf(v.z, wt, sum.z);
+                sum.w = fmaf(v.w, wt, sum.w);
             }
         }
-        reinterpret_cast<float4 *>(red)[threadIdx.x] = acc;
+        red[threadIdx.x] = sum;
         __syncthreads();
         if (slice == 0 && item < kItems) {
-            float4 sum = acc;
             for (int sl = 1; sl < kSlices; ++sl) {
-                const float4 v = reinterpret_cast<const float4 *>(red)[threadIdx.x + sl * kLanesPerSlice];
+                const float4 v = red[threadIdx.x + sl * kLanesPerSlice];
                 sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
             }
             const int h = item / 32, d4 = item % 32;
@@ -369,8 +394,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 
     allow_dependent_launch();
     unsigned char *stages = smem + warp * kStages * kStageBytes;
-    uint64_t *bars =
-        reinterpret_cast<uint64_t *>(smem + kWarps * kStages * kStageBytes) + warp * kStages;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOffset) + warp * kStages;
     if (lane == 0) {
         if (warp == 0) {
             prefetch_tensormap(&tmap_k);
@@ -410,9 +434,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     const int n_chunks = max(0, (tok1 - tok0 + kChunkTokens - 1) / kChunkTokens);
     const int my_chunks = (n_chunks > warp) ? (n_chunks - 1 - warp) / kWarps + 1 : 0;
 
-    int *stage_rows =
-        reinterpret_cast<int *>(smem + kWarps * kStages * kStageBytes + kWarps * kStages * 8) +
-        warp * kStages;
+    int *stage_rows = reinterpret_cast<int *>(smem + kRowsOffset) + warp * kStages;
     __syncwarp();
 
     // The chunk holding position T-1 is written by the prologue this kernel
@@ -456,13 +478,13 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     for (int k = 0; k < kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
     // Only the first kPrewaitChunks chunks of each warp are requested before
-    // griddepcontrol.wait: the rest would queue in the memory system ahead of
-    // the previous layer's merge and this layer's query loads, which sit on
-    // the critical path of the layer chain.
+    // griddepcontrol.wait: in the fused step the rest would queue in the
+    // memory system ahead of the previous layer's merge and this layer's
+    // query loads, which sit on the critical path of the layer chain.
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && k < kPrewaitChunks && !holds_new_token(k))
+            if (k < first && k < kPrewaitChunks<kFused> && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
 
@@ -482,7 +504,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     HeadRope rope;
     float gain_q[4], gain_k[4];
     if (has_q || new_chunk >= 0)
-        rope.init(pos, p.inv_freq);
+        rope.init(pos, p.freqs);
     if (has_q)
         load_head(p.gamma_q, gain_q);
     if (new_chunk >= 0)
@@ -510,7 +532,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && (k >= kPrewaitChunks || holds_new_token(k)))
+            if (k < first && (k >= kPrewaitChunks<kFused> || holds_new_token(k)))
                 issue(k, first_phys[k], policy);
     }
     __syncwarp();
@@ -555,8 +577,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     // group's stages are refilled together once it has been folded.
     bool ok = true;
     int k0 = 0;
-    for (; k0 < my_chunks; k0 += kStages) {
-        const int nc = min(kStages, my_chunks - k0);
+    for (int nc; k0 < my_chunks; k0 += nc) {
+        nc = min(kStages, my_chunks - k0);
         uint32_t stage_addr[kStages];
         int rows[kStages];
 #pragma unroll
@@ -611,7 +633,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 #pragma unroll
         for (int c = 0; c < kStages; ++c) {
             const int k = k0 + c + kStages;
-            if (k < my_chunks) {
+            if (c < nc && k < my_chunks) {
                 const int phys = phys_of(k);
                 if (lane == 0) {
                     fence_proxy_async_smem();
@@ -678,8 +700,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     // 0's release; its acquire (when last) orders the other CTAs' stores
     // before the merge's loads, which the second barrier extends to all
     // threads.
-    unsigned *ticket_slot = reinterpret_cast<unsigned *>(
-        smem + kWarps * kStages * kStageBytes + kWarps * kStages * 8 + kWarps * kStages * 4);
+    unsigned *ticket_slot = reinterpret_cast<unsigned *>(smem + kTicketOffset);
     __syncthreads();
     unsigned *ticket = p.tickets + static_cast<size_t>(b) * p.Hkv + kvh;
     if (threadIdx.x == 0)
@@ -687,7 +708,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncthreads();
     if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
         return;
-    merge_in_last_cta<G>(p, b, kvh, n_parts, reinterpret_cast<float *>(smem));
+    merge_in_last_cta<G>(p, b, kvh, n_parts, smem, reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
     if (threadIdx.x == 0)
         *ticket = 0u; // ready for the next call
 }
@@ -939,7 +960,11 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
-    kp.fused_merge = a.num_partitions <= kFusedMergeMax ? 1 : 0;
+    kp.fused_merge = a.num_partitions <= kFusedMergeMax &&
+                             static_cast<long>(G) * a.num_partitions * kHeadDim * 4 + kMergeScratchBytes <=
+                                 kStageAreaBytes
+                         ? 1
+                         : 0;
     if (a.fused) {
         kp.q_raw = a.q_raw;
         kp.k_new = a.k_new;
@@ -950,8 +975,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
         kp.v_cache = const_cast<uint16_t *>(a.v_cache);
         kp.q_out = a.q_out;
         kp.eps = a.eps;
-        for (int i = 0; i < kHeadDim / 2; ++i)
-            kp.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / kHeadDim);
+        kp.freqs = make_rope_freqs(a.rope_theta);
     }
     if (a.num_partitions > 1) {
         const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;

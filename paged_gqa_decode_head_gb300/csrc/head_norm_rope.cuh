@@ -11,6 +11,8 @@
 // to ~1e-7 rad even at pos ~ 1e5 where an fp32 product would be off by ~1e-2.
 #pragma once
 
+#include <cmath>
+
 #include "common.cuh"
 
 namespace pgqa {
@@ -35,15 +37,37 @@ __device__ __forceinline__ void rope_angle(int pos, double inv_freq, float &cs, 
     sincosf(static_cast<float>(r), &sn, &cs);
 }
 
+// The RoPE frequencies omega_i = theta^(-2i/128) as r^i, r = theta^(-2/128),
+// from the six powers r^(2^k) (k = 0..5): lane l forms omega_l and
+// omega_(l+32) with at most six fp64 products (relative error ~1e-15), and
+// every lane reads the same six values, which a per-lane table index into
+// kernel parameters would serialise.
+struct RopeFreqs {
+    double r_pow2[6]; // r^(2^k)
+};
+
+inline RopeFreqs make_rope_freqs(double theta)
+{
+    RopeFreqs f;
+    for (int k = 0; k < 6; ++k)
+        f.r_pow2[k] = std::pow(theta, -2.0 * (1 << k) / kHeadDim);
+    return f;
+}
+
 // The rotation of this lane's two pairs (lane, lane + 64) and
-// (lane + 32, lane + 96) at position pos; inv_freq[i] = theta^(-2i/128).
+// (lane + 32, lane + 96) at position pos.
 struct HeadRope {
     float cs[2], sn[2];
-    __device__ __forceinline__ void init(int pos, const double *inv_freq)
+    __device__ __forceinline__ void init(int pos, const RopeFreqs &f)
     {
         const int lane = threadIdx.x & 31;
-        rope_angle(pos, inv_freq[lane], cs[0], sn[0]);
-        rope_angle(pos, inv_freq[lane + 32], cs[1], sn[1]);
+        double w = 1.0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k)
+            if ((lane >> k) & 1)
+                w *= f.r_pow2[k];
+        rope_angle(pos, w, cs[0], sn[0]);
+        rope_angle(pos, w * f.r_pow2[5], cs[1], sn[1]);
     }
 };
 
@@ -83,10 +107,10 @@ __device__ __forceinline__ void norm_rope_apply(float (&x)[4], const float (&gai
 
 // x[i] (dim lane + 32 i) of RoPE_pos(RMSNorm(src) * gamma); whole warp.
 __device__ __forceinline__ void norm_rope_head(const uint16_t *src, const uint16_t *gamma, float eps,
-                                               int pos, const double *inv_freq, float (&x)[4])
+                                               int pos, const RopeFreqs &freqs, float (&x)[4])
 {
     HeadRope rope;
-    rope.init(pos, inv_freq);
+    rope.init(pos, freqs);
     float gain[4];
     load_head(gamma, gain);
     load_head(src, x);

@@ -23,7 +23,6 @@ namespace {
 __device__ unsigned g_flags_prologue;
 
 constexpr int kWarpsPerBlock = 4;
-constexpr int kHalf = kHeadDim / 2;
 
 struct PrologueParams {
     const uint16_t *q, *k, *v, *gamma_q, *gamma_k;
@@ -31,7 +30,7 @@ struct PrologueParams {
     uint16_t *k_cache, *v_cache, *q_out;
     int B, Hq, Hkv, P, max_pages, num_pages;
     float eps;
-    double inv_freq[kHalf]; // theta^(-2i/D), i < D/2
+    RopeFreqs freqs;
 };
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
@@ -81,7 +80,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
     }
 
     float x[4];
-    norm_rope_head(src, gamma, p.eps, pos, p.inv_freq, x);
+    norm_rope_head(src, gamma, p.eps, pos, p.freqs, x);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         dst[lane + 32 * i] = f32_to_bf16_bits(x[i]);
@@ -111,8 +110,7 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
     p.max_pages = a.max_pages;
     p.num_pages = a.num_pages;
     p.eps = a.eps;
-    for (int i = 0; i < kHalf; ++i)
-        p.inv_freq[i] = std::pow(a.rope_theta, -2.0 * i / kHeadDim);
+    p.freqs = make_rope_freqs(a.rope_theta);
     const long items = static_cast<long>(a.B) * (a.Hq + a.Hkv);
     const unsigned blocks = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
     return launch_pdl(prologue_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);

@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention KV GB/s (fraction of HBM peak); µs per layer-step at T=8K"
 WORKLOAD = "qwen3_0p6b_t8k"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_split_kernel_qwen3_t8k.md")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_kernel_qwen3_t8k.md")
 
 
 def parse_args():
@@ -48,7 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
-    ap.add_argument("--layers", type=int, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers per step (default 28); a smaller count is only for profiling captures")
     return ap.parse_args()
 
 
@@ -267,8 +268,14 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     kv_bytes = sum(kv_bytes_layer(int(kv.context_lens.sum())) for kv, _ in layers)
-    algo_bytes_layer = (kv_bytes_layer(w["T"]) + 2 * w["Hq"] * 128 + 4 * math.ceil(w["T"] / 16)
-                        + 6 * w["Hq"] * 128)
+    Hq, Hkv = w["Hq"], w["Hkv"]
+    # algorithmic bytes of one decode_step_paged launch (one layer): the K+V
+    # history, the new token's q, k, v and the two gains read, the block
+    # table, the appended K and V rows, the rotated q and both outputs written
+    algo_bytes_step = (kv_bytes_layer(w["T"]) + 2 * (Hq + 2 * Hkv) * 128 + 2 * 2 * 128 + 4 * math.ceil(w["T"] / 16)
+                       + 2 * 2 * Hkv * 128 + 2 * Hq * 128 + 6 * Hq * 128)
+    # attention alone (decode_attn_paged): history, q, table, outputs
+    algo_bytes_attn = kv_bytes_layer(w["T"]) + 2 * Hq * 128 + 4 * math.ceil(w["T"] / 16) + 6 * Hq * 128
 
     def barrier():
         if world > 1:
@@ -343,7 +350,8 @@ def run_ours(args, rank, world, local):
     step_s = ms / args.steps / 1e3
     value = world * kv_bytes / step_s / 1e9
     layer_attn_s = ms_attn / args.steps / 1e3 / n_layers
-    achieved = algo_bytes_layer / layer_attn_s / 1e9
+    achieved = algo_bytes_step / (step_s / n_layers) / 1e9
+    achieved_attn = algo_bytes_attn / layer_attn_s / 1e9
     peak, peak_kind = load_peaks()
     e2e_s = ms_e2e / e2e_steps / 1e3
     # one decode_step_paged kernel per layer; the library merges up to 64
@@ -362,9 +370,13 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2: 896 MiB of KV, each layer's 32 MiB read once per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": profiled_traffic(),
-                     "kernel": "decode_mma_kernel (split-KV attention with in-kernel merge), timed as an "
-                               "attention-only graph of "
-                               f"{n_layers} layers, CUDA events on the launch stream"},
+                     "kernel": "decode_mma_kernel<2, fused> (decode_step_paged: prologue, split-KV attention, "
+                               f"in-kernel merge), {n_layers} launches per step graph, CUDA events on the launch "
+                               "stream; achieved = algorithmic bytes of one launch / (step time / launches)",
+                     "bytes_per_launch": algo_bytes_step,
+                     "attention_only": {"achieved": achieved_attn, "frac": achieved_attn / peak,
+                                        "bytes_per_launch": algo_bytes_attn,
+                                        "kernel": "decode_mma_kernel<2> (decode_attn_paged), attention-only graph"}},
         "e2e": {"value": world * kv_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * n_layers * launches_per_layer,

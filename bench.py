@@ -48,6 +48,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, "ragged_b64", "long_split_kv_t128k", "host_tiled_t64k"],
+                    help="the headline step (default) or one of the larger parity workloads, "
+                         "measured on their own (one JSON line per variant, not the headline line)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default 28); a smaller count is only for profiling captures")
     return ap.parse_args()
@@ -391,6 +395,107 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_secondary(args):
+    """Bandwidth of one of the larger workloads: KV bytes per second of
+    decode_attn_paged (ragged batch, long split-KV context), or bytes per second
+    over the host link of the host-tiled copy pipeline and of the zero-copy
+    variant, each against its own roofline (measured HBM copy bandwidth, or a
+    256 MiB pinned host-to-device copy timed in the same run)."""
+    import numpy as np
+    import torch
+
+    import paged_gqa_decode_head_gb300 as pg
+    from paged_gqa_decode_head_gb300 import inputs
+    from paged_gqa_decode_head_gb300.runner import to_device_bf16, to_device_i32
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pg.load_library()
+    w = inputs.WORKLOADS[args.workload]
+    scale = 1.0 / math.sqrt(128)
+    peak, peak_kind = load_peaks()
+    iters = max(3, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / iters / 1e3
+
+    def emit(variant, nbytes, s, roof_peak, roof_unit, roof_kind, extra):
+        gbs = nbytes / s / 1e9
+        line = {"metric": f"{args.workload} {variant}", "value": gbs, "unit": "GB/s", "us": s * 1e6,
+                "workload": args.workload, "variant": variant, "steps": iters, "data": "synthetic",
+                "roofline": {"achieved": gbs, "peak": roof_peak, "unit": roof_unit, "frac": gbs / roof_peak,
+                             "peak_kind": roof_kind}}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    if args.workload in ("ragged_b64", "long_split_kv_t128k"):
+        if args.workload == "ragged_b64":
+            kv, q = inputs.ragged_b64()
+            nps = [0]
+        else:
+            kv, q = inputs.long_split_kv()
+            nps = [w["T"] // w["partition"], 0]
+        B, Hq, Hkv = len(kv.context_lens), w["Hq"], w["Hkv"]
+        qd = to_device_bf16(q, dev)
+        kc, vc = to_device_bf16(kv.k_cache, dev), to_device_bf16(kv.v_cache, dev)
+        bt, ctx = to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev)
+        out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+        kv_bytes = 4 * int(kv.context_lens.sum()) * Hkv * 128
+        for npr in nps:
+            n = pg.decode_attn_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, npr)
+            ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+            np_used = pg.decode_attn_partition_count(B, Hkv, kv.page_size, kv.max_pages, npr)
+            s = timed(lambda: pg.decode_attn_paged(qd, kc, vc, bt, ctx, scale, out_f32=out, workspace=ws,
+                                                   num_partitions=npr))
+            emit(f"decode_attn_paged NP={np_used}" + (" (automatic)" if npr == 0 else " (workload's 512-position partitions)"),
+                 kv_bytes, s, peak, "GB/s", peak_kind,
+                 {"config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "kv_bytes": kv_bytes,
+                             "l2": "inputs larger than L2"}})
+        assert pg.device_error_flags() == 0
+        return
+
+    # host_tiled_t64k: the copy pipeline and the zero-copy variant
+    q, k, v = inputs.host_tiled_kv()
+    B, Hq, Hkv, T, tile = w["B"], w["Hq"], w["Hkv"], w["T"], w["tile"]
+    hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    nbytes = 2 * hk.numel() * 2
+    probe = torch.empty(hk.numel(), dtype=torch.bfloat16, device=dev)
+    link = max(hk.numel() * 2 / timed(lambda: probe.copy_(hk.view(-1), non_blocking=True)) / 1e9 for _ in range(3))
+    del probe
+    qd = to_device_bf16(q, dev)
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    n_slots = 2
+    slots_k = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
+    slots_v = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
+    events = [torch.cuda.Event() for _ in range(2 * n_slots)]
+    m = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    l = torch.empty_like(m)
+    acc = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    copy_stream = torch.cuda.Stream(dev)
+    s = timed(lambda: pg.attn_host_tiled_run(qd, hk, hv, scale, slots_k, slots_v, events, m, l, acc, out_f32=out,
+                                             tile_len=tile, copy_stream=copy_stream))
+    cfg = {"B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "host_bytes": nbytes,
+           "link_probe": "256 MiB pinned host-to-device cudaMemcpyAsync, best of 3"}
+    emit(f"attn_host_tiled_run ({tile}-position tiles, {n_slots} slots)", nbytes, s, link, "GB/s", "measured link",
+         {"config": cfg})
+    n = pg.attn_host_direct_workspace_size(B, Hq, Hkv, T, 0)
+    ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+    np_used = pg.attn_host_direct_partition_count(B, Hkv, T, 0)
+    s = timed(lambda: pg.attn_host_direct(qd, hk, hv, scale, out_f32=out, workspace=ws))
+    emit(f"attn_host_direct (zero-copy, NP={np_used})", nbytes, s, link, "GB/s", "measured link", {"config": cfg})
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -398,6 +503,9 @@ def main():
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload != WORKLOAD:
+        if rank == 0:
+            run_secondary(args)
     else:
         run_ours(args, rank, world, local)
 

@@ -246,6 +246,35 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
                         cudaStream_t copy_stream);
 
 /*
+ * Zero-copy variant of the host-tiled attention ([EdgeTransformerEngine],
+ * KV-offload design, whose state (m, l, acc) and exact merge it keeps): the
+ * history stays in pinned host memory and the kernel reads it over the host
+ * link directly, with no device tiles and no copies. The history is split
+ * into num_partitions ranges of consecutive positions, one CTA per (range, KV
+ * head, sequence); their states are merged exactly as in
+ * attn_partition_merge.
+ *
+ *   q            [B][Hq][D] bf16, device memory
+ *   host_k, host_v  [B][T][Hkv][D] bf16, pinned host memory mapped into the
+ *                device address space (cudaHostAlloc, or cudaHostRegister
+ *                with mapping); PGQA_ERR_INVALID_ARG if it is not. The caller
+ *                keeps it alive and unmodified until the stream passes the
+ *                call.
+ *   num_partitions  0 = automatic (one wave of CTAs, ranges >= 512
+ *                positions), else the requested count (clamped to [1, T]).
+ *   workspace    device scratch of ws_bytes >= attn_host_direct_workspace_size
+ *                (may be NULL when that size is 0); no initial value needed.
+ *   out_f32, out_bf16  [B][Hq][D], at least one non-NULL.
+ * T = 0 produces zeros. Reads q after the previous kernel in the stream
+ * completes (programmatic stream serialisation).
+ */
+int attn_host_direct_partition_count(int B, int Hkv, int T, int num_partitions);
+size_t attn_host_direct_workspace_size(int B, int Hq, int Hkv, int T, int num_partitions);
+int attn_host_direct(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v, int T,
+                     int B, int Hq, int Hkv, int D, float scale, int num_partitions, float *out_f32,
+                     pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * decode_attn_paged_static -- decode_attn_paged for callers that cannot
  * allocate device memory. The pages have no counterpart of this entry point;
  * it exists for code that runs where cudaMalloc is not allowed (inside an

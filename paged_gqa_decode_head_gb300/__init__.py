@@ -7,6 +7,9 @@ raises if the library is missing (there is no CPU fallback).
 """
 from .binding import (  # noqa: F401
     PgqaError,
+    attn_host_direct,
+    attn_host_direct_partition_count,
+    attn_host_direct_workspace_size,
     attn_host_tiled_run,
     attn_partition_merge,
     attn_tile_finalize,

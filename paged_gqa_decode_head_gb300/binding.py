@@ -33,6 +33,9 @@ EXPORTED = (
     "attn_tile_update",
     "attn_tile_finalize",
     "attn_host_tiled_run",
+    "attn_host_direct_partition_count",
+    "attn_host_direct_workspace_size",
+    "attn_host_direct",
     "decode_attn_paged_static",
 )
 
@@ -95,6 +98,12 @@ def load_library():
         lib.attn_tile_finalize.restype = I
         lib.attn_host_tiled_run.argtypes = [P, P, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P, P, P, P]
         lib.attn_host_tiled_run.restype = I
+        lib.attn_host_direct_partition_count.argtypes = [I, I, I, I]
+        lib.attn_host_direct_partition_count.restype = I
+        lib.attn_host_direct_workspace_size.argtypes = [I, I, I, I, I]
+        lib.attn_host_direct_workspace_size.restype = S
+        lib.attn_host_direct.argtypes = [P, P, P, I, I, I, I, I, F, I, P, P, P, S, P]
+        lib.attn_host_direct.restype = I
         lib.decode_attn_paged_static.argtypes = [P] * 5 + [I] * 7 + [F, I, P, P, P]
         lib.decode_attn_paged_static.restype = I
         _lib = lib
@@ -278,6 +287,39 @@ def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, event
         _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
         _stream(compute_stream), _stream(copy_stream))
     _check("attn_host_tiled_run", st)
+
+
+def attn_host_direct_partition_count(B: int, Hkv: int, T: int, num_partitions: int = 0) -> int:
+    n = load_library().attn_host_direct_partition_count(B, Hkv, T, num_partitions)
+    if n < 0:
+        _check("attn_host_direct_partition_count", n)
+    return n
+
+
+def attn_host_direct_workspace_size(B: int, Hq: int, Hkv: int, T: int, num_partitions: int = 0) -> int:
+    return int(load_library().attn_host_direct_workspace_size(B, Hq, Hkv, T, num_partitions))
+
+
+def attn_host_direct(q, host_k, host_v, scale: float, out_f32=None, out_bf16=None, workspace=None,
+                     num_partitions: int = 0, stream=None) -> None:
+    """Zero-copy attention over a history in pinned host memory.
+
+    q: device bf16 [B, Hq, D]; host_k/host_v: pinned CPU bf16 [B, T, Hkv, D]."""
+    lib = load_library()
+    bf = torch.bfloat16
+    B, Hq, D = q.shape
+    Bk, T, Hkv, Dk = host_k.shape
+    if tuple(host_v.shape) != tuple(host_k.shape) or Bk != B or Dk != D:
+        raise ValueError("attn_host_direct: host_k and host_v must both be [B, T, Hkv, D]")
+    ws_ptr = _dev(workspace, torch.uint8, "workspace", nullable=True)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    hk = _host(host_k, bf, "host_k") if T > 0 else None
+    hv = _host(host_v, bf, "host_v") if T > 0 else None
+    st = lib.attn_host_direct(_dev(q, bf, "q"), hk, hv, T, B, Hq,
+                              Hkv, D, float(scale), int(num_partitions),
+                              _dev(out_f32, torch.float32, "out_f32", nullable=True),
+                              _dev(out_bf16, bf, "out_bf16", nullable=True), ws_ptr, ws_bytes, _stream(stream))
+    _check("attn_host_direct", st)
 
 
 STATIC_SCRATCH_BYTES = 8 << 20  # PGQA_STATIC_SCRATCH_BYTES in include/pgqa.h

@@ -484,4 +484,73 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
     return attn_tile_finalize(m, l, acc, B, Hq, D, out_f32, out_bf16, compute_stream);
 }
 
+int attn_host_direct_partition_count(int B, int Hkv, int T, int num_partitions)
+{
+    if (B < 0 || Hkv <= 0 || T < 0 || num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "attn_host_direct_partition_count: bad sizes");
+    return pgqa::host_direct_partitions(B, Hkv, T, num_partitions, sm_count_current_device());
+}
+
+size_t attn_host_direct_workspace_size(int B, int Hq, int Hkv, int T, int num_partitions)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || T < 0 || num_partitions < 0)
+        return 0;
+    const int np = pgqa::host_direct_partitions(B, Hkv, T, num_partitions, sm_count_current_device());
+    return pgqa::host_direct_workspace_bytes(B, Hq, np);
+}
+
+int attn_host_direct(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v, int T,
+                     int B, int Hq, int Hkv, int D, float scale, int num_partitions, float *out_f32,
+                     pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "attn_host_direct";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (T < 0 || num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: need T >= 0 and num_partitions >= 0", fn);
+    if (!std::isfinite(scale))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (static_cast<long long>(B) * T * Hkv > (1LL << 40))
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: B * T * Hkv too large", fn);
+    if (B == 0)
+        return ok();
+    if (!q || (T > 0 && (!host_k || !host_v)) || (!out_f32 && !out_bf16))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned16(q) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) ||
+        !aligned16(host_k) || !aligned16(host_v) || (workspace && !aligned16(workspace)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte alignment", fn);
+    // The history must be pinned host memory mapped into the device address
+    // space; its device-side address is what the kernel reads through.
+    void *dk = nullptr, *dv = nullptr;
+    if (T > 0) {
+        if (cudaHostGetDevicePointer(&dk, const_cast<pgqa_bf16 *>(host_k), 0) != cudaSuccess ||
+            cudaHostGetDevicePointer(&dv, const_cast<pgqa_bf16 *>(host_v), 0) != cudaSuccess || !dk || !dv) {
+            cudaGetLastError();
+            return fail(PGQA_ERR_INVALID_ARG, "%s: host_k / host_v are not mapped pinned host memory", fn);
+        }
+    }
+    const int np = pgqa::host_direct_partitions(B, Hkv, T, num_partitions, sm_count_current_device());
+    const size_t need = pgqa::host_direct_workspace_bytes(B, Hq, np);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu", fn,
+                    need, np, workspace ? ws_bytes : static_cast<size_t>(0));
+    pgqa::HostDirectArgs a{};
+    a.q = q;
+    a.k = static_cast<const pgqa_bf16 *>(dk);
+    a.v = static_cast<const pgqa_bf16 *>(dv);
+    a.T = T;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale = scale;
+    a.num_partitions = np;
+    a.out_f32 = out_f32;
+    a.out_bf16 = out_bf16;
+    a.ws = static_cast<float *>(workspace);
+    cudaError_t err = pgqa::launch_host_direct(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
 } // extern "C"

@@ -901,16 +901,40 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
     if (requested > 0) {
         np = requested;
     } else {
-        // Fill every CTA slot of one wave, keep partitions between 128 and
-        // 1024 positions (long enough to amortise the merge, short enough to
-        // balance ragged batches).
+        // Pick NP minimising waves x (positions per CTA + a per-CTA cost):
+        // with (b, KV head) units = B * Hkv and one CTA per SM, a wave runs
+        // `slots` CTAs, each streaming ceil(max_pages / NP) pages; starting a
+        // CTA (table and context loads, the first request's latency) costs
+        // about as much as streaming kCtaCostPositions positions. Partitions
+        // stay at least 128 positions long so the merge is amortised, and at
+        // most ~4096 positions when the units alone fill a wave (the model
+        // counts every sequence at max_pages, which overstates the work of a
+        // ragged batch and would pick too few partitions).
+        // The cost constant fits NP sweeps on GB300: B = 1 (T = 8192, 131072)
+        // wants one full wave (NP = 19), B = 2 NP = 9, B = 4 NP = 4, B = 16
+        // NP = 1, and B = 64 ragged contexts up to 32768 any NP from 4 to 12
+        // (NP = 2: 4 % slower).
+        constexpr long kCtaCostPositions = 600;
         const long units = static_cast<long>(B) * Hkv;
         const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * kCtasPerSm;
-        long ppp = (units * max_pages + slots - 1) / slots;
         const long lo = std::max(1, 128 / page_size);
-        const long hi = std::max(1, 1024 / page_size);
-        ppp = std::min(std::max(ppp, lo), hi);
-        np = (max_pages + ppp - 1) / ppp;
+        const long max_np = std::max<long>(1, std::min<long>((max_pages + lo - 1) / lo, 2 * slots));
+        const long hi_pages = std::max(1, 4096 / page_size);
+        const long min_np = units >= slots ? std::min(max_np, (max_pages + hi_pages - 1) / hi_pages) : 1;
+        long best = 0;
+        double best_cost = 0.0;
+        for (long n = min_np; n <= max_np; ++n) {
+            const long ppp = (max_pages + n - 1) / n;
+            if (n > min_np && (max_pages + ppp - 1) / ppp != n)
+                continue; // the same split as a smaller n
+            const long waves = (units * n + slots - 1) / slots;
+            const double cost = static_cast<double>(waves) * (ppp * page_size + kCtaCostPositions);
+            if (best == 0 || cost < best_cost) {
+                best = n;
+                best_cost = cost;
+            }
+        }
+        np = best;
     }
     np = std::min<long>(std::max<long>(np, 1), std::min(max_pages, kMaxPartitions));
     const long ppp = (max_pages + np - 1) / np;

@@ -58,10 +58,26 @@ struct TileArgs {
     float *m, *l, *acc;
 };
 
+struct HostDirectArgs {
+    const pgqa_bf16 *q, *k, *v; // k, v: device-side addresses of mapped host memory
+    int T, B, Hq, Hkv;
+    float scale;
+    int num_partitions; // resolved, >= 1
+    float *out_f32;
+    pgqa_bf16 *out_bf16;
+    float *ws; // partition states when num_partitions > 1
+};
+
+// Shortest partition of the zero-copy variant (positions).
+constexpr int kHostDirectMinPositions = 512;
+
 // Largest partition count the merge supports.
 constexpr int kMaxPartitions = 65536;
 
 cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream);
+int host_direct_partitions(int B, int Hkv, int T, int requested, int sm_count);
+size_t host_direct_workspace_bytes(int B, int Hq, int num_partitions);
+cudaError_t launch_host_direct(const HostDirectArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream);
 cudaError_t launch_tile_init(float *m, float *l, float *acc, int B, int Hq, cudaStream_t stream);

@@ -123,3 +123,16 @@ def test_partition_choice(lib):
     assert pg.decode_attn_workspace_size(1, 16, 8, 128, 16, 512, 1) == 0
     ws = pg.decode_attn_workspace_size(1, 16, 8, 128, 16, 512, 4)
     assert ws >= 1 * 16 * 4 * (128 + 2) * 4
+
+
+def test_host_direct_validation(lib):
+    F = ctypes.c_float
+    # missing pointers, bad head dim, bad sizes are refused before any launch
+    assert lib.attn_host_direct(None, None, None, 64, 1, 16, 8, 128, F(0.1), 0, None, None, None, 0, None) == -1
+    assert lib.attn_host_direct(None, None, None, 64, 1, 16, 8, 64, F(0.1), 0, None, None, None, 0, None) == -2
+    assert lib.attn_host_direct(None, None, None, -1, 1, 16, 8, 128, F(0.1), 0, None, None, None, 0, None) == -1
+    base = 0x10000000
+    assert lib.attn_host_direct(base, base + 4, base, 64, 1, 16, 8, 128, F(0.1), 0, base, None, None, 0,
+                                None) == -3
+    # B = 0 is a valid no-op
+    assert lib.attn_host_direct(None, None, None, 64, 0, 16, 8, 128, F(0.1), 0, None, None, None, 0, None) == 0

@@ -8,8 +8,10 @@
  *     append of the new token's K/V into the paged cache;
  *   - decode attention with (m, l, acc) online softmax, split over KV
  *     partitions and merged exactly;
+ *   - both in one launch per layer (decode_step_paged);
  *   - a host-tiled variant that keeps (m, l, acc) in global memory while KV
- *     tiles are streamed in from pinned host memory.
+ *     tiles are streamed in from pinned host memory, and a zero-copy variant
+ *     that reads a history held in pinned host memory directly.
  *
  * Sources (page title, section):
  *   "From Qwen3 math to CUDA kernels: a 0.6B inference runtime"
@@ -76,7 +78,7 @@ enum pgqa_status {
 /* Sticky device-side flags (bit mask) read by pgqa_device_error(). */
 #define PGQA_DEVERR_BAD_PAGE 1u     /* block-table entry outside [0, num_pages) */
 #define PGQA_DEVERR_BAD_CONTEXT 2u  /* context length < 0 (or < 1 for the prologue) or too long */
-#define PGQA_DEVERR_WAIT_TIMEOUT 4u /* an asynchronous copy did not complete in time */
+#define PGQA_DEVERR_WAIT_TIMEOUT 4u /* a bounded wait (an asynchronous copy) ran out */
 
 /* Message of the calling thread's last failing call ("" if none). */
 const char *pgqa_last_error(void);
@@ -84,6 +86,17 @@ const char *pgqa_last_error(void);
 /* Read the sticky device flags of the current device into *flags_out (OR of
  * PGQA_DEVERR_*) and clear them if clear != 0. Synchronises the device. */
 int pgqa_device_error(unsigned *flags_out, int clear);
+
+/*
+ * pgqa_selftest_wait_timeout -- exercises the library's failure path for a
+ * wait that never completes (no counterpart on the pages): one CTA waits on
+ * an mbarrier that nothing arrives on; the wait gives up after its limit
+ * (200 ms), the kernel raises PGQA_DEVERR_WAIT_TIMEOUT and returns, and the
+ * context stays usable. Enqueued on `stream`; read the flag with
+ * pgqa_device_error. Every wait in the library's kernels is bounded the same
+ * way.
+ */
+int pgqa_selftest_wait_timeout(cudaStream_t stream);
 
 /*
  * qk_norm_rope_append -- fused decode prologue for one layer.
@@ -188,6 +201,43 @@ int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v
                       int page_size, int max_pages, int num_pages, float rope_theta, float eps,
                       float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
                       void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Multi-query decode: M >= 1 new tokens per sequence decoded in one step
+ * (speculative or multi-token-prediction verification). Token i (0 <= i < M)
+ * of sequence b sits at position T_b - M + i, where context_lens[b] = T_b
+ * counts all M new tokens, and attends causally to positions
+ * 0 .. T_b - M + i: the same s2.6 attention as decode_attn_paged, once per
+ * new token, with each token's own prefix. M = 1 is exactly the
+ * single-token step.
+ *
+ * qk_norm_rope_append_multi -- the prologue for M tokens: as
+ *   qk_norm_rope_append with q [B][M][Hq][D], k, v [B][M][Hkv][D] and q_out
+ *   [B][M][Hq][D]; token i is rotated at position T_b - M + i and appended to
+ *   its slot. Needs T_b >= M (else the sequence is skipped, flag raised).
+ *   1 <= M <= 64.
+ * decode_attn_paged_multi -- the attention for M tokens: q [B][M][Hq][D] (the
+ *   prologue's q_out), out_f32 / out_bf16 [B][M][Hq][D]; other arguments as
+ *   decode_attn_paged. One CTA serves the M x g (token, head) pairs of a KV
+ *   head, so M * (Hq / Hkv) <= 8 (else PGQA_ERR_UNSUPPORTED). Sequences with
+ *   T_b < M produce zeros (flag raised). The attention kernel reads the
+ *   cache rows of positions below T_b - M before the previous kernel in the
+ *   stream completes (programmatic serialisation), the M new rows after.
+ * decode_attn_multi_workspace_size -- workspace bytes for the same arguments.
+ */
+int qk_norm_rope_append_multi(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                              const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                              const int32_t *context_lens, const int32_t *block_table,
+                              pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int M,
+                              int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                              float rope_theta, float eps, cudaStream_t stream);
+size_t decode_attn_multi_workspace_size(int B, int M, int Hq, int Hkv, int D, int page_size,
+                                        int max_pages, int num_partitions);
+int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+                            const int32_t *block_table, const int32_t *context_lens, int B, int M,
+                            int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                            float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * attn_partition_merge -- exact merge of NP partition states (s9.1).

@@ -63,6 +63,10 @@ def _load():
         lib.oracle_qk_norm_rope_append.argtypes = [P] * 10 + [I] * 7 + [D, D]
         lib.oracle_qk_norm_rope_append.restype = I
         lib.oracle_decode_attention.argtypes = [P] * 5 + [I] * 7 + [D, P]
+        lib.oracle_decode_attention_multi.argtypes = [P] * 5 + [I] * 8 + [D, P]
+        lib.oracle_decode_attention_multi.restype = I
+        lib.oracle_qk_norm_rope_append_multi.argtypes = [P] * 10 + [I] * 8 + [D, D]
+        lib.oracle_qk_norm_rope_append_multi.restype = I
         lib.oracle_decode_attention.restype = I
         lib.oracle_attention_contiguous.argtypes = [P, P, P, I, L, I, I, I, D, P]
         lib.oracle_attention_contiguous.restype = I
@@ -208,6 +212,43 @@ def decode_attention(q, k_cache, v_cache, block_table, context_lens, scale: floa
     st = lib.oracle_decode_attention(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(ctx), B, Hq, Hkv, D, P,
                                      bt.shape[1], num_pages, float(scale), _ptr(out))
     _check(st, "decode_attention")
+    return out
+
+
+def qk_norm_rope_append_multi(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache,
+                              page_size: int, rope_theta: float, eps: float = 1e-6):
+    """Prologue for M new tokens per sequence at positions T-M .. T-1.
+
+    q: u16 [B,M,Hq,D]; k, v: u16 [B,M,Hkv,D]. Returns (q_out [B,M,Hq,D], k_cache', v_cache')."""
+    lib = _load()
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    gq, gk = _u16(gamma_q), _u16(gamma_k)
+    ctx, bt = _i32(context_lens), _i32(block_table)
+    kc = _u16(k_cache).copy()
+    vc = _u16(v_cache).copy()
+    B, M, Hq, D = q.shape
+    Hkv = k.shape[2]
+    q_out = np.zeros_like(q)
+    st = lib.oracle_qk_norm_rope_append_multi(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ctx), _ptr(bt), _ptr(kc), _ptr(vc),
+        _ptr(q_out), B, M, Hq, Hkv, D, page_size, bt.shape[1], kc.shape[0], float(rope_theta), float(eps))
+    _check(st, "qk_norm_rope_append_multi")
+    return q_out, kc, vc
+
+
+def decode_attention_multi(q, k_cache, v_cache, block_table, context_lens, scale: float) -> np.ndarray:
+    """Multi-query decode attention: token i of M (q [B,M,Hq,D]) attends causally to
+    positions 0 .. T-M+i. Returns float64 [B, M, Hq, D]."""
+    lib = _load()
+    q, kc, vc = _u16(q), _u16(k_cache), _u16(v_cache)
+    bt, ctx = _i32(block_table), _i32(context_lens)
+    B, M, Hq, D = q.shape
+    num_pages, Hkv, P, D2 = kc.shape
+    assert D2 == D
+    out = np.zeros((B, M, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_attention_multi(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(ctx), B, M, Hq, Hkv, D,
+                                           P, bt.shape[1], num_pages, float(scale), _ptr(out))
+    _check(st, "decode_attention_multi")
     return out
 
 

@@ -230,6 +230,69 @@ int oracle_qk_norm_rope_append(const uint16_t *q, const uint16_t *k, const uint1
     return status;
 }
 
+/* The prologue for M new tokens per sequence: token i of sequence b (q row
+ * [b][i][h], k and v rows [b][i][h]) sits at position T - M + i and gets the
+ * same treatment as the single new token of oracle_qk_norm_rope_append at
+ * that position (q_out [B][M][Hq][D]; K slot rotated, V slot copied).
+ * Returns ORACLE_BAD_ARG for T < M or an unusable slot. */
+int oracle_qk_norm_rope_append_multi(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     const uint16_t *gamma_q, const uint16_t *gamma_k,
+                                     const int32_t *context_lens, const int32_t *block_table,
+                                     uint16_t *k_cache, uint16_t *v_cache, uint16_t *q_out, int B,
+                                     int M, int Hq, int Hkv, int D, int P, int max_pages,
+                                     int num_pages, double theta, double eps)
+{
+    if (B < 0 || M < 1 || Hq <= 0 || Hkv <= 0 || D <= 0 || (D % 2) != 0 || P <= 0 ||
+        Hq % Hkv != 0)
+        return ORACLE_BAD_ARG;
+    double *x = malloc(sizeof(double) * (size_t)D * 4);
+    if (!x)
+        return ORACLE_NO_MEMORY;
+    double *gam = x + D, *nrm = x + 2 * D, *rot = x + 3 * D;
+    int status = ORACLE_OK;
+    for (int b = 0; b < B && status == ORACLE_OK; ++b) {
+        long T = context_lens[b];
+        if (T < M || T > (long)max_pages * P) {
+            status = ORACLE_BAD_ARG;
+            break;
+        }
+        for (int i = 0; i < M && status == ORACLE_OK; ++i) {
+            long pos = T - M + i;
+            long tok = (long)b * M + i;
+            for (int h = 0; h < Hq; ++h) {
+                for (int r = 0; r < D; ++r) {
+                    x[r] = oracle_bf16_to_double(q[(tok * Hq + h) * D + r]);
+                    gam[r] = oracle_bf16_to_double(gamma_q[r]);
+                }
+                oracle_head_rmsnorm(x, gam, D, eps, nrm);
+                oracle_rope_half(nrm, D, pos, theta, rot);
+                for (int r = 0; r < D; ++r)
+                    q_out[(tok * Hq + h) * D + r] = oracle_round_bf16(rot[r]);
+            }
+            for (int h = 0; h < Hkv; ++h) {
+                long off = oracle_cache_offset(block_table, max_pages, num_pages, b, h, pos, Hkv, P,
+                                               D);
+                if (off < 0) {
+                    status = ORACLE_BAD_ARG;
+                    break;
+                }
+                for (int r = 0; r < D; ++r) {
+                    x[r] = oracle_bf16_to_double(k[(tok * Hkv + h) * D + r]);
+                    gam[r] = oracle_bf16_to_double(gamma_k[r]);
+                }
+                oracle_head_rmsnorm(x, gam, D, eps, nrm);
+                oracle_rope_half(nrm, D, pos, theta, rot);
+                for (int r = 0; r < D; ++r) {
+                    k_cache[off + r] = oracle_round_bf16(rot[r]);
+                    v_cache[off + r] = v[(tok * Hkv + h) * D + r];
+                }
+            }
+        }
+    }
+    free(x);
+    return status;
+}
+
 /* ------------------------------------------------------------------------- */
 /* A5 + A6: decode attention, full softmax [Qwen3 runtime s2.5, s2.6]        */
 /* ------------------------------------------------------------------------- */
@@ -318,6 +381,68 @@ int oracle_decode_attention(const uint16_t *q, const uint16_t *k_cache, const ui
             for (int r = 0; r < D; ++r)
                 qv[r] = oracle_bf16_to_double(q[((long)b * Hq + h) * D + r]);
             softmax_attend(qv, keys, values, T, D, scale, scores, out + ((long)b * Hq + h) * D);
+        }
+    }
+    free(keys), free(values), free(scores), free(qv);
+    return status;
+}
+
+/* Multi-query decode: M new tokens per sequence. With T = context_lens[b]
+ * (counting all M new tokens), token i (0 <= i < M) sits at position
+ * t_i = T - M + i and, being causal (j <= t_i), attends to positions
+ * 0 .. t_i, i.e. to the first T - M + i + 1 keys: for each (b, i, h),
+ * softmax_attend over those keys of KV head h / (Hq/Hkv). q and out are
+ * [B][M][Hq][D]. Returns ORACLE_BAD_ARG for T < M. */
+int oracle_decode_attention_multi(const uint16_t *q, const uint16_t *k_cache,
+                                  const uint16_t *v_cache, const int32_t *block_table,
+                                  const int32_t *context_lens, int B, int M, int Hq, int Hkv,
+                                  int D, int P, int max_pages, int num_pages, double scale,
+                                  double *out)
+{
+    if (B < 0 || M < 1 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv != 0)
+        return ORACLE_BAD_ARG;
+    long Tmax = 0;
+    for (int b = 0; b < B; ++b) {
+        if (context_lens[b] < M || (long)context_lens[b] > (long)max_pages * P)
+            return ORACLE_BAD_ARG;
+        if (context_lens[b] > Tmax)
+            Tmax = context_lens[b];
+    }
+    size_t n = (size_t)(Tmax > 0 ? Tmax : 1);
+    double *keys = malloc(sizeof(double) * n * (size_t)D);
+    double *values = malloc(sizeof(double) * n * (size_t)D);
+    double *scores = malloc(sizeof(double) * n);
+    double *qv = malloc(sizeof(double) * (size_t)D);
+    if (!keys || !values || !scores || !qv) {
+        free(keys), free(values), free(scores), free(qv);
+        return ORACLE_NO_MEMORY;
+    }
+    int status = ORACLE_OK;
+    for (int b = 0; b < B && status == ORACLE_OK; ++b) {
+        long T = context_lens[b];
+        for (int h = 0; h < Hq && status == ORACLE_OK; ++h) {
+            int kvh = oracle_kv_head(h, Hq, Hkv);
+            for (long j = 0; j < T; ++j) {
+                long off = oracle_cache_offset(block_table, max_pages, num_pages, b, kvh, j, Hkv,
+                                               P, D);
+                if (off < 0) {
+                    status = ORACLE_BAD_ARG;
+                    break;
+                }
+                for (int r = 0; r < D; ++r) {
+                    keys[j * D + r] = oracle_bf16_to_double(k_cache[off + r]);
+                    values[j * D + r] = oracle_bf16_to_double(v_cache[off + r]);
+                }
+            }
+            if (status != ORACLE_OK)
+                break;
+            for (int i = 0; i < M; ++i) {
+                long row = ((long)b * M + i) * Hq + h;
+                for (int r = 0; r < D; ++r)
+                    qv[r] = oracle_bf16_to_double(q[row * D + r]);
+                long visible = T - M + i + 1; /* positions 0 .. t_i */
+                softmax_attend(qv, keys, values, visible, D, scale, scores, out + row * D);
+            }
         }
     }
     free(keys), free(values), free(scores), free(qv);

@@ -15,7 +15,9 @@ from .binding import (  # noqa: F401
     attn_tile_finalize,
     attn_tile_init,
     attn_tile_update,
+    decode_attn_multi_workspace_size,
     decode_attn_paged,
+    decode_attn_paged_multi,
     decode_attn_paged_static,
     decode_step_paged,
     decode_attn_partition_count,
@@ -24,4 +26,5 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
     qk_norm_rope_append,
+    qk_norm_rope_append_multi,
 )

@@ -23,11 +23,15 @@ _lib = None
 EXPORTED = (
     "pgqa_last_error",
     "pgqa_device_error",
+    "pgqa_selftest_wait_timeout",
     "qk_norm_rope_append",
     "decode_attn_partition_count",
     "decode_attn_workspace_size",
     "decode_attn_paged",
     "decode_step_paged",
+    "qk_norm_rope_append_multi",
+    "decode_attn_multi_workspace_size",
+    "decode_attn_paged_multi",
     "attn_partition_merge",
     "attn_tile_init",
     "attn_tile_update",
@@ -79,6 +83,12 @@ def load_library():
         lib.pgqa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
         lib.pgqa_device_error.restype = I
         lib.qk_norm_rope_append.argtypes = [P] * 10 + [I] * 7 + [F, F, P]
+        lib.qk_norm_rope_append_multi.argtypes = [P] * 10 + [I] * 8 + [F, F, P]
+        lib.qk_norm_rope_append_multi.restype = I
+        lib.decode_attn_multi_workspace_size.argtypes = [I] * 8
+        lib.decode_attn_multi_workspace_size.restype = S
+        lib.decode_attn_paged_multi.argtypes = [P] * 5 + [I] * 8 + [F, I, P, P, P, S, P]
+        lib.decode_attn_paged_multi.restype = I
         lib.qk_norm_rope_append.restype = I
         lib.decode_attn_partition_count.argtypes = [I] * 5
         lib.decode_attn_partition_count.restype = I
@@ -104,6 +114,8 @@ def load_library():
         lib.attn_host_direct_workspace_size.restype = S
         lib.attn_host_direct.argtypes = [P, P, P, I, I, I, I, I, F, I, P, P, P, S, P]
         lib.attn_host_direct.restype = I
+        lib.pgqa_selftest_wait_timeout.argtypes = [P]
+        lib.pgqa_selftest_wait_timeout.restype = I
         lib.decode_attn_paged_static.argtypes = [P] * 5 + [I] * 7 + [F, I, P, P, P]
         lib.decode_attn_paged_static.restype = I
         _lib = lib
@@ -198,6 +210,47 @@ def decode_attn_paged(q, k_cache, v_cache, block_table, context_lens, scale: flo
         _dev(out_f32, torch.float32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
         ws_ptr, ws_bytes, _stream(stream))
     _check("decode_attn_paged", st)
+
+
+def qk_norm_rope_append_multi(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache, q_out,
+                              rope_theta: float, eps: float = 1e-6, stream=None) -> None:
+    """Prologue for M new tokens per sequence: q [B, M, Hq, D], k/v [B, M, Hkv, D]."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    B, M, Hq, D = q.shape
+    Hkv = k.shape[2]
+    num_pages, _, P, _ = k_cache.shape
+    st = lib.qk_norm_rope_append_multi(
+        _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(gamma_q, bf, "gamma_q"),
+        _dev(gamma_k, bf, "gamma_k"), _dev(context_lens, i32, "context_lens"),
+        _dev(block_table, i32, "block_table"), _dev(k_cache, bf, "k_cache"), _dev(v_cache, bf, "v_cache"),
+        _dev(q_out, bf, "q_out"), B, M, Hq, Hkv, D, P, block_table.shape[1], num_pages,
+        float(rope_theta), float(eps), _stream(stream))
+    _check("qk_norm_rope_append_multi", st)
+
+
+def decode_attn_multi_workspace_size(B: int, M: int, Hq: int, Hkv: int, D: int, page_size: int, max_pages: int,
+                                     num_partitions: int = 0) -> int:
+    return int(load_library().decode_attn_multi_workspace_size(B, M, Hq, Hkv, D, page_size, max_pages,
+                                                                num_partitions))
+
+
+def decode_attn_paged_multi(q, k_cache, v_cache, block_table, context_lens, scale: float, out_f32=None,
+                            out_bf16=None, workspace=None, num_partitions: int = 0, stream=None) -> None:
+    """Attention for M new tokens per sequence: q and outputs [B, M, Hq, D]."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    B, M, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_cache.shape
+    ws_ptr = _dev(workspace, torch.uint8, "workspace", nullable=True)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.decode_attn_paged_multi(
+        _dev(q, bf, "q"), _dev(k_cache, bf, "k_cache"), _dev(v_cache, bf, "v_cache"),
+        _dev(block_table, i32, "block_table"), _dev(context_lens, i32, "context_lens"), B, M, Hq, Hkv, D, P,
+        block_table.shape[1], num_pages, float(scale), int(num_partitions),
+        _dev(out_f32, torch.float32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
+        ws_ptr, ws_bytes, _stream(stream))
+    _check("decode_attn_paged_multi", st)
 
 
 def decode_step_paged(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache, scale: float,
@@ -320,6 +373,11 @@ def attn_host_direct(q, host_k, host_v, scale: float, out_f32=None, out_bf16=Non
                               _dev(out_f32, torch.float32, "out_f32", nullable=True),
                               _dev(out_bf16, bf, "out_bf16", nullable=True), ws_ptr, ws_bytes, _stream(stream))
     _check("attn_host_direct", st)
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Run the bounded-wait self-test kernel (raises DEVERR_WAIT_TIMEOUT on the device)."""
+    _check("pgqa_selftest_wait_timeout", load_library().pgqa_selftest_wait_timeout(_stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 8 << 20  # PGQA_STATIC_SCRATCH_BYTES in include/pgqa.h

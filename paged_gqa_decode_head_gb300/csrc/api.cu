@@ -14,6 +14,7 @@
 
 namespace pgqa {
 constexpr int kHeadDimHost = 128;
+constexpr int kMaxGroupHost = 8; // columns (query, head pairs) one decode CTA serves
 }
 
 namespace {
@@ -123,20 +124,29 @@ int pgqa_device_error(unsigned *flags_out, int clear)
     return ok();
 }
 
-int qk_norm_rope_append(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+int pgqa_selftest_wait_timeout(cudaStream_t stream)
+{
+    cudaError_t err = pgqa::launch_wait_selftest(stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, "pgqa_selftest_wait_timeout");
+    return ok();
+}
+
+static int prologue_impl(const char *fn, int M, const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
                         const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
                         const int32_t *context_lens, const int32_t *block_table,
                         pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq,
                         int Hkv, int D, int page_size, int max_pages, int num_pages,
                         float rope_theta, float eps, cudaStream_t stream)
 {
-    const char *fn = "qk_norm_rope_append";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
     if (int st = check_pages(fn, page_size, max_pages, num_pages))
         return st;
     if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps))
         return fail(PGQA_ERR_INVALID_ARG, "%s: rope_theta must be > 0 and eps >= 0", fn);
+    if (M < 1 || M > 64)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: M = %d new tokens per sequence outside [1, 64]", fn, M);
     if (B == 0)
         return ok();
     if (!q || !k || !v || !gamma_q || !gamma_k || !context_lens || !block_table || !k_cache ||
@@ -148,11 +158,35 @@ int qk_norm_rope_append(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
     pgqa::PrologueArgs a{q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache,
                          q_out, B, Hq, Hkv, page_size, max_pages, num_pages,
-                         static_cast<double>(rope_theta), eps};
+                         static_cast<double>(rope_theta), eps, M};
     cudaError_t err = pgqa::launch_prologue(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
     return ok();
+}
+
+int qk_norm_rope_append(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                        const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                        const int32_t *context_lens, const int32_t *block_table,
+                        pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq,
+                        int Hkv, int D, int page_size, int max_pages, int num_pages,
+                        float rope_theta, float eps, cudaStream_t stream)
+{
+    return prologue_impl("qk_norm_rope_append", 1, q, k, v, gamma_q, gamma_k, context_lens, block_table,
+                         k_cache, v_cache, q_out, B, Hq, Hkv, D, page_size, max_pages, num_pages, rope_theta,
+                         eps, stream);
+}
+
+int qk_norm_rope_append_multi(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                              const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                              const int32_t *context_lens, const int32_t *block_table,
+                              pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int M,
+                              int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                              float rope_theta, float eps, cudaStream_t stream)
+{
+    return prologue_impl("qk_norm_rope_append_multi", M, q, k, v, gamma_q, gamma_k, context_lens, block_table,
+                         k_cache, v_cache, q_out, B, Hq, Hkv, D, page_size, max_pages, num_pages, rope_theta,
+                         eps, stream);
 }
 
 int decode_attn_partition_count(int B, int Hkv, int page_size, int max_pages, int num_partitions)
@@ -174,19 +208,23 @@ size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, 
     return pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
 }
 
-int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+static int attn_impl(const char *fn, int M, const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
                       const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
                       int Hkv, int D, int page_size, int max_pages, int num_pages, float scale,
                       int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
                       size_t ws_bytes, cudaStream_t stream)
 {
-    const char *fn = "decode_attn_paged";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
     if (int st = check_pages(fn, page_size, max_pages, num_pages))
         return st;
     if (num_partitions < 0)
         return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
+    if (M < 1)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: M = %d new tokens per sequence, need >= 1", fn, M);
+    if (M * (Hq / Hkv) > pgqa::kMaxGroupHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: M * (Hq / Hkv) = %d exceeds %d", fn, M * (Hq / Hkv),
+                    pgqa::kMaxGroupHost);
     if (!std::isfinite(scale))
         return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
     if (static_cast<long long>(num_pages) * Hkv * page_size > 0x7FFFFFFFLL)
@@ -203,7 +241,7 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
+    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, M * Hq, np);
     if (need > 0 && (!workspace || ws_bytes < need))
         return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu",
                     fn, need, np, workspace ? ws_bytes : static_cast<size_t>(0));
@@ -225,10 +263,41 @@ int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_b
     a.out_f32 = out_f32;
     a.out_bf16 = out_bf16;
     a.ws = static_cast<float *>(workspace);
+    a.M = M;
     cudaError_t err = pgqa::launch_decode(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
     return ok();
+}
+
+int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+                      const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
+                      int Hkv, int D, int page_size, int max_pages, int num_pages, float scale,
+                      int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
+                      size_t ws_bytes, cudaStream_t stream)
+{
+    return attn_impl("decode_attn_paged", 1, q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv, D,
+                     page_size, max_pages, num_pages, scale, num_partitions, out_f32, out_bf16, workspace,
+                     ws_bytes, stream);
+}
+
+int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
+                            const int32_t *block_table, const int32_t *context_lens, int B, int M,
+                            int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                            float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                            void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    return attn_impl("decode_attn_paged_multi", M, q, k_cache, v_cache, block_table, context_lens, B, Hq, Hkv,
+                     D, page_size, max_pages, num_pages, scale, num_partitions, out_f32, out_bf16, workspace,
+                     ws_bytes, stream);
+}
+
+size_t decode_attn_multi_workspace_size(int B, int M, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                        int num_partitions)
+{
+    if (M < 1)
+        return 0;
+    return decode_attn_workspace_size(B, M * Hq, Hkv, D, page_size, max_pages, num_partitions);
 }
 
 int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,

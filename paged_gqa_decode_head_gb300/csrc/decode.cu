@@ -86,6 +86,7 @@ struct SplitParams {
     float *ws_m, *ws_l, *ws_acc;
     unsigned *tickets; // [B*Hkv] partition tickets (fused merge)
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
+    int G, M; // group size; new tokens per sequence (column n = query n / G, head n % G)
     int fused_merge;
     float scale_log2;
     // fused decode step only: the new token's raw heads and the prologue's
@@ -95,6 +96,17 @@ struct SplitParams {
     float eps;
     RopeFreqs freqs;
 };
+
+// Row (of the [B][M][Hq] query / output arrays) of column n of KV head kvh;
+// with one new token (kMulti = false) the columns are the heads kvh*G + n.
+template <bool kMulti>
+__device__ __forceinline__ size_t column_row(const SplitParams &p, int b, int kvh, int n)
+{
+    if constexpr (kMulti)
+        return (static_cast<size_t>(b) * p.M + n / p.G) * p.Hq + kvh * p.G + n % p.G;
+    else
+        return static_cast<size_t>(b) * p.Hq + kvh * p.G + n;
+}
 
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p)
 {
@@ -107,19 +119,25 @@ __device__ __forceinline__ uint32_t ld_u32(const uint16_t *p)
 // O^T += V^T P^T (A = 16 dims x 16 keys of V^T, B = P^T). Lane (g, t) =
 // (lane / 4, lane % 4) holds heads 2t and 2t+1 (valid when < G) for keys g
 // and g+8 of a chunk, and O^T rows (dims) 16mt+g and 16mt+g+8.
-template <int G> struct MmaWarp {
-    uint32_t qb0[8], qb1[8]; // B = Q^T: head g, dims 16ks+2t..+1 and 16ks+8+2t..+1 (bf16x2)
+//
+// The NCOL <= 8 columns are (query, head) pairs: the g query heads of the KV
+// head for the single-token step, and (query i, head h) at column i*g + h
+// when M new tokens are decoded at once.
+template <int NCOL> struct MmaWarp {
+    uint32_t qb0[8], qb1[8]; // B = Q^T: column g, dims 16ks+2t..+1 and 16ks+8+2t..+1 (bf16x2)
     float o[8][4];           // O^T m-tile mt: [dim 16mt+g][2t], [..][2t+1], [dim 16mt+g+8][2t], [..][2t+1]
-    float m[2];              // running max of heads 2t, 2t+1 (base-2 units)
-    float l[2];              // sum of p of heads 2t, 2t+1 over this lane's keys
+    float m[2];              // running max of columns 2t, 2t+1 (base-2 units)
+    float l[2];              // sum of p of columns 2t, 2t+1 over this lane's keys
 
-    __device__ __forceinline__ void init(const uint16_t *q_rows)
+    // q_row: the query row of this lane's column g (lane / 4), or NULL when
+    // g >= NCOL.
+    __device__ __forceinline__ void init(const uint16_t *q_row)
     {
-        const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+        const int lane = threadIdx.x & 31, t = lane & 3;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            qb0[ks] = g < G ? ld_u32(q_rows + g * kHeadDim + 16 * ks + 2 * t) : 0u;
-            qb1[ks] = g < G ? ld_u32(q_rows + g * kHeadDim + 16 * ks + 8 + 2 * t) : 0u;
+            qb0[ks] = q_row ? ld_u32(q_row + 16 * ks + 2 * t) : 0u;
+            qb1[ks] = q_row ? ld_u32(q_row + 16 * ks + 8 + 2 * t) : 0u;
         }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
@@ -129,11 +147,12 @@ template <int G> struct MmaWarp {
     }
 
     // Fold NC resident chunks at once (their MMAs and loads interleave):
-    // stage[c] is the shared address of chunk c's four swizzled boxes and
-    // rows[c] (1..16) its valid rows; later rows are masked out.
-    template <int NC>
-    __device__ __forceinline__ void fold(const uint32_t (&stage)[kStages], const int (&rows)[kStages],
-                                         float scale_log2)
+    // stage[c] is the shared address of chunk c's four swizzled boxes; keys
+    // from row lim0[c] (lim1[c]) on are masked out for column 2t (2t+1) --
+    // the chunk's valid rows, cut further by a column's causal limit.
+    template <int NC, bool kPerColumn>
+    __device__ __forceinline__ void fold(const uint32_t (&stage)[kStages], const int (&lim0)[kStages],
+                                         const int (&lim1)[kStages], float scale_log2)
     {
         const int lane = threadIdx.x & 31, g = lane >> 2;
         const int mq = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row within it
@@ -158,17 +177,28 @@ template <int G> struct MmaWarp {
                 mma_bf16_16816((ks & 1) ? sb[c] : sa[c], a, qb0[ks], qb1[ks]);
             }
         }
-        // sc[c][e]: e = 0 (key g, head 2t), 1 (key g, 2t+1), 2 (key g+8, 2t), 3 (key g+8, 2t+1)
+        // sc[c][e]: e = 0 (key g, column 2t), 1 (key g, 2t+1), 2 (key g+8, 2t), 3 (key g+8, 2t+1)
         float sc[NC][4];
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 sc[c][e] = (sa[c][e] + sb[c][e]) * scale_log2;
-            if (g >= rows[c])
-                sc[c][0] = sc[c][1] = -INFINITY;
-            if (g + 8 >= rows[c])
-                sc[c][2] = sc[c][3] = -INFINITY;
+            if constexpr (kPerColumn) {
+                if (g >= lim0[c])
+                    sc[c][0] = -INFINITY;
+                if (g >= lim1[c])
+                    sc[c][1] = -INFINITY;
+                if (g + 8 >= lim0[c])
+                    sc[c][2] = -INFINITY;
+                if (g + 8 >= lim1[c])
+                    sc[c][3] = -INFINITY;
+            } else { // every column has the chunk's valid rows, lim0
+                if (g >= lim0[c])
+                    sc[c][0] = sc[c][1] = -INFINITY;
+                if (g + 8 >= lim0[c])
+                    sc[c][2] = sc[c][3] = -INFINITY;
+            }
         }
         float mn[2];
         bool grow = false;
@@ -234,7 +264,7 @@ template <int G> struct MmaWarp {
     }
 
     // Warp totals: reduce l over the 8 lanes sharing t; write the record
-    // [G][128] O, then [G] m, then [G] l.
+    // [NCOL][128] O, then [NCOL] m, then [NCOL] l.
     __device__ __forceinline__ void store_record(float *rec)
     {
         const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -247,15 +277,15 @@ template <int G> struct MmaWarp {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             const int h = 2 * t + c;
-            if (h < G) {
+            if (h < NCOL) {
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     rec[h * kHeadDim + 16 * mt + g] = o[mt][c];
                     rec[h * kHeadDim + 16 * mt + g + 8] = o[mt][2 + c];
                 }
                 if (g == 0) {
-                    rec[G * kHeadDim + h] = m[c];
-                    rec[G * kHeadDim + G + h] = l[c];
+                    rec[NCOL * kHeadDim + h] = m[c];
+                    rec[NCOL * kHeadDim + NCOL + h] = l[c];
                 }
             }
         }
@@ -277,17 +307,16 @@ template <int G> struct MmaWarp {
 // accumulators into shared memory (one bulk copy per head) while one warp per
 // head loads m and l and forms the weights e^(m_p - M) and L with shuffles;
 // then every thread folds its share of the accumulators from shared memory.
-template <int G>
+template <int NCOL, bool kMulti>
 __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, unsigned char *smem,
                                   uint64_t *bar)
 {
     constexpr int kThreads = kWarps * 32;
-    float *acc = reinterpret_cast<float *>(smem);         // [G][n][128]
-    float *w = acc + static_cast<size_t>(G) * n * kHeadDim; // [G][kFusedMergeMax] weights
-    float *Ls = w + G * kFusedMergeMax;                     // [G], padded to 16 floats
+    float *acc = reinterpret_cast<float *>(smem);            // [NCOL][n][128]
+    float *w = acc + static_cast<size_t>(NCOL) * n * kHeadDim; // [NCOL][kFusedMergeMax] weights
+    float *Ls = w + NCOL * kFusedMergeMax;                     // [NCOL], padded to 16 floats
     float4 *red = reinterpret_cast<float4 *>(Ls + 16);      // [kThreads] partial sums
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -296,15 +325,15 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, u
         fence_proxy_async_smem();
         fence_proxy_async_global();
         const uint32_t row_bytes = static_cast<uint32_t>(n) * kHeadDim * 4;
-        mbar_arrive_expect_tx(bar, G * row_bytes);
+        mbar_arrive_expect_tx(bar, NCOL * row_bytes);
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int h = 0; h < NCOL; ++h)
             bulk_copy_g2s_nohint(acc + static_cast<size_t>(h) * n * kHeadDim,
-                                 p.ws_acc + (row0 + h) * p.NP * kHeadDim, row_bytes, bar);
+                                 p.ws_acc + column_row<kMulti>(p, b, kvh, h) * p.NP * kHeadDim, row_bytes, bar);
     }
-    for (int h = warp; h < G; h += kWarps) {
-        const float *mh = p.ws_m + (row0 + h) * p.NP;
-        const float *lh = p.ws_l + (row0 + h) * p.NP;
+    for (int h = warp; h < NCOL; h += kWarps) {
+        const float *mh = p.ws_m + column_row<kMulti>(p, b, kvh, h) * p.NP;
+        const float *lh = p.ws_l + column_row<kMulti>(p, b, kvh, h) * p.NP;
         const float m0 = lane < n ? __ldcg(mh + lane) : kEmptyMax;
         const float m1 = lane + 32 < n ? __ldcg(mh + lane + 32) : kEmptyMax;
         const float l0 = lane < n ? __ldcg(lh + lane) : 0.f;
@@ -332,7 +361,7 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, u
         (void)mbar_wait_bounded(bar, 0);
         return;
     }
-    constexpr int kItems = G * 32; // (head, 4 dims)
+    constexpr int kItems = NCOL * 32; // (column, 4 dims)
     constexpr int kSlices = kThreads >= kItems ? kThreads / kItems : 1;
     constexpr int kLanesPerSlice = kThreads / kSlices;
     for (int base = 0; base < kItems; base += kLanesPerSlice) {
@@ -362,7 +391,7 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, u
             const float L = Ls[h];
             const float inv = L > 0.f ? 1.f / L : 0.f;
             const float r[4] = {sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv};
-            const size_t off = (row0 + h) * kHeadDim + 4 * d4;
+            const size_t off = column_row<kMulti>(p, b, kvh, h) * kHeadDim + 4 * d4;
             if (p.out_f32)
                 *reinterpret_cast<float4 *>(p.out_f32 + off) = make_float4(r[0], r[1], r[2], r[3]);
             if (p.out_bf16)
@@ -378,7 +407,9 @@ __device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, u
 // query heads it serves; the warp whose chunk holds position T-1 computes the
 // new K row, appends K and V to the cache and patches the row into its staged
 // chunk, so every history chunk can be requested before griddepcontrol.wait.
-template <int G, bool kFused>
+// NCOL = M * G columns; kMulti: M > 1 new tokens (not fused), each column
+// with its own causal limit.
+template <int NCOL, bool kFused, bool kMulti>
 __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const SplitParams p)
@@ -420,7 +451,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         tbl_val = (chunk_token(lane) < tok0 + part_tokens && page < p.max_pages) ? table[page] : -1;
     }
     int T = p.context_lens[b];
-    if (T < (kFused ? 1 : 0) || T > p.max_pages * p.P) {
+    // M new tokens sit at positions T - M .. T - 1 (M = 1: the decode step)
+    if (T < (kFused || p.M > 1 ? p.M : 0) || T > p.max_pages * p.P) {
         if (part == 0 && threadIdx.x == 0)
             raise_flag(PGQA_DEVERR_BAD_CONTEXT);
         T = 0;
@@ -437,11 +469,12 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     int *stage_rows = reinterpret_cast<int *>(smem + kRowsOffset) + warp * kStages;
     __syncwarp();
 
-    // The chunk holding position T-1 is written by the prologue this kernel
-    // may overlap, so it is requested only after griddepcontrol.wait (the
-    // fused step patches that row into shared memory itself instead).
+    // Chunks holding the new positions T - M .. T - 1 are written by the
+    // prologue this kernel may overlap, so they are requested only after
+    // griddepcontrol.wait (the fused step patches its row into shared memory
+    // itself instead).
     auto holds_new_token = [&](int k) {
-        return !kFused && chunk_token(k) + kChunkTokens > T - 1;
+        return !kFused && chunk_token(k) + kChunkTokens > T - p.M;
     };
     // Physical pages of this warp's chunks, 32 at a time: lane L caches the
     // entry of chunk 32*blk + L. Called by the whole (converged) warp.
@@ -491,7 +524,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     // fused step: what the prologue needs that no earlier kernel writes
     // (gains, rotation, the append slot) is prepared before the wait.
     const int pos = T - 1;
-    const bool has_q = kFused && T > 0 && warp < G;
+    const bool has_q = kFused && T > 0 && warp < NCOL; // fused: NCOL = G
     int new_chunk = -1; // index k of the chunk holding pos in this warp's sequence, or -1
     int new_phys = -1;
     if (kFused && T > 0 && pos >= tok0 && pos < tok1) {
@@ -514,11 +547,12 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 
     // The new token's q, k, v come from the previous kernels: load them now,
     // ahead of the remaining bulk requests.
-    const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * G + warp) * kHeadDim;
+    const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * NCOL + warp) * kHeadDim;
     const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
     float xq[4], xk[4];
     uint16_t new_v[4] = {0, 0, 0, 0};
-    MmaWarp<G> st;
+    MmaWarp<NCOL> st;
+    const int col = lane >> 2; // this lane's B-operand column
     if (has_q)
         load_head(p.q_raw + qrow, xq);
     if (new_chunk >= 0) {
@@ -528,7 +562,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
             new_v[i] = p.v_new[krow + lane + 32 * i];
     }
     if constexpr (!kFused)
-        st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
+        st.init(col < NCOL ? p.q + column_row<kMulti>(p, b, kvh, col) * kHeadDim : nullptr);
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
@@ -570,7 +604,18 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
             }
         }
         __syncthreads();
-        st.init(q_buf);
+        st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
+    }
+
+    // Causal limit (exclusive position) of this lane's columns 2t and 2t+1:
+    // query i sees positions up to T - M + i.
+    int qlim0 = T, qlim1 = T;
+    if constexpr (kMulti) {
+        const int c_lo = 2 * (lane & 3);
+        if (c_lo < NCOL)
+            qlim0 = T - p.M + 1 + c_lo / p.G;
+        if (c_lo + 1 < NCOL)
+            qlim1 = T - p.M + 1 + (c_lo + 1) / p.G;
     }
 
     // Chunks are consumed in groups of up to kStages (one per stage); the
@@ -580,12 +625,12 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     for (int nc; k0 < my_chunks; k0 += nc) {
         nc = min(kStages, my_chunks - k0);
         uint32_t stage_addr[kStages];
-        int rows[kStages];
+        int rows[kStages], lim0[kStages], lim1[kStages];
 #pragma unroll
         for (int c = 0; c < kStages; ++c) {
             const int k = k0 + c;
             stage_addr[c] = smem_addr(stages + (k % kStages) * kStageBytes);
-            rows[c] = 0;
+            rows[c] = lim0[c] = lim1[c] = 0;
             if (c < nc) {
                 const bool landed = mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1);
                 if (!__all_sync(0xFFFFFFFFu, landed))
@@ -604,6 +649,12 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                         *reinterpret_cast<uint16_t *>(stage + 2 * kBoxBytes + off) = new_v[i];
                     }
                     __syncwarp();
+                }
+                lim0[c] = rows[c];
+                lim1[c] = rows[c];
+                if constexpr (kMulti) {
+                    lim0[c] = min(rows[c], qlim0 - chunk_token(k));
+                    lim1[c] = min(rows[c], qlim1 - chunk_token(k));
                 }
                 if (rows[c] < kChunkTokens) {
                     // Rows past the history (all rows of a chunk whose page
@@ -624,11 +675,11 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         if (!ok)
             break;
         if (nc == 3)
-            st.template fold<3>(stage_addr, rows, p.scale_log2);
+            st.template fold<3, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
         else if (nc == 2)
-            st.template fold<2>(stage_addr, rows, p.scale_log2);
+            st.template fold<2, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
         else
-            st.template fold<1>(stage_addr, rows, p.scale_log2);
+            st.template fold<1, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < kStages; ++c) {
@@ -658,25 +709,24 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     st.store_record(reinterpret_cast<float *>(stages));
     __syncthreads();
 
-    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
-    for (int e = threadIdx.x; e < G * kHeadDim; e += kWarps * 32) {
+    for (int e = threadIdx.x; e < NCOL * kHeadDim; e += kWarps * 32) {
         const int h = e / kHeadDim;
         const int d = e % kHeadDim;
         float M = kEmptyMax;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-            M = fmaxf(M, rec[G * kHeadDim + h]);
+            M = fmaxf(M, rec[NCOL * kHeadDim + h]);
         }
         float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-            const float wt = exp2f(rec[G * kHeadDim + h] - M);
-            L = fmaf(rec[G * kHeadDim + G + h], wt, L);
+            const float wt = exp2f(rec[NCOL * kHeadDim + h] - M);
+            L = fmaf(rec[NCOL * kHeadDim + NCOL + h], wt, L);
             O = fmaf(rec[h * kHeadDim + d], wt, O);
         }
-        const size_t row = row0 + h;
+        const size_t row = column_row<kMulti>(p, b, kvh, h);
         if (n_parts == 1) {
             const float o = L > 0.f ? O / L : 0.f;
             if (p.out_f32)
@@ -708,7 +758,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncthreads();
     if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
         return;
-    merge_in_last_cta<G>(p, b, kvh, n_parts, smem, reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
+    merge_in_last_cta<NCOL, kMulti>(p, b, kvh, n_parts, smem, reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
     if (threadIdx.x == 0)
         *ticket = 0u; // ready for the next call
 }
@@ -716,6 +766,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 struct MergeParams {
     const float *m, *l, *acc;
     int Hq, NP;
+    int M; // query rows per sequence are M * Hq (M new tokens)
     float *out_f32;
     uint16_t *out_bf16;
     const int32_t *context_lens;
@@ -744,7 +795,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     grid_dependency_wait();
     int np = p.NP;
     if (p.context_lens) {
-        const int b = row / p.Hq;
+        const int b = row / (p.M * p.Hq);
         int T = p.context_lens[b];
         if (T < 0 || T > p.max_pages * p.P)
             T = 0;
@@ -860,7 +911,7 @@ cudaError_t encode_cache_map(CUtensorMap *map, const void *base, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G, bool kFused>
+template <int NCOL, bool kFused, bool kMulti>
 cudaError_t launch_split_t(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
                            dim3 grid, cudaStream_t stream)
 {
@@ -870,23 +921,25 @@ cudaError_t launch_split_t(const CUtensorMap &mk, const CUtensorMap &mv, const S
     if (err != cudaSuccess)
         return err;
     if (dev >= kMaxDevices || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_mma_kernel<G, kFused>,
+        err = cudaFuncSetAttribute(decode_mma_kernel<NCOL, kFused, kMulti>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < kMaxDevices)
             configured[dev] = true;
     }
-    return launch_pdl(decode_mma_kernel<G, kFused>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk,
+    return launch_pdl(decode_mma_kernel<NCOL, kFused, kMulti>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk,
                       mv, kp);
 }
 
-template <int G>
+template <int NCOL>
 cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
                          dim3 grid, bool fused, cudaStream_t stream)
 {
-    return fused ? launch_split_t<G, true>(mk, mv, kp, grid, stream)
-                 : launch_split_t<G, false>(mk, mv, kp, grid, stream);
+    if (kp.M > 1)
+        return launch_split_t<NCOL, false, true>(mk, mv, kp, grid, stream);
+    return fused ? launch_split_t<NCOL, true, false>(mk, mv, kp, grid, stream)
+                 : launch_split_t<NCOL, false, false>(mk, mv, kp, grid, stream);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -948,7 +1001,8 @@ size_t decode_ticket_bytes(int B, int Hkv)
 
 // Workspace (NP > 1): partition tickets [B*Hkv] (zero before first use;
 // every completed call leaves them zero), then m, l [B*Hq*NP] and acc
-// [B*Hq*NP*128] (fp32, no initial value needed).
+// [B*Hq*NP*128] (fp32, no initial value needed); with M new tokens per
+// sequence pass M * Hq as Hq.
 size_t decode_workspace_bytes(int B, int Hkv, int Hq, int num_partitions)
 {
     if (num_partitions <= 1)
@@ -961,6 +1015,8 @@ size_t decode_workspace_bytes(int B, int Hkv, int Hq, int num_partitions)
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
 {
     const int G = a.Hq / a.Hkv;
+    const int M = a.M > 0 ? a.M : 1;
+    const int NCOL = G * M; // (query, head) columns of one KV head, <= 8 (checked by the caller)
     CUtensorMap mk, mv;
     const long long rows = static_cast<long long>(a.num_pages) * a.Hkv * a.page_size;
     if (rows == 0)
@@ -985,7 +1041,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
     kp.fused_merge = a.num_partitions <= kFusedMergeMax &&
-                             static_cast<long>(G) * a.num_partitions * kHeadDim * 4 + kMergeScratchBytes <=
+                             static_cast<long>(NCOL) * a.num_partitions * kHeadDim * 4 + kMergeScratchBytes <=
                                  kStageAreaBytes
                          ? 1
                          : 0;
@@ -1002,7 +1058,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
         kp.freqs = make_rope_freqs(a.rope_theta);
     }
     if (a.num_partitions > 1) {
-        const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;
+        const size_t n = static_cast<size_t>(a.B) * M * a.Hq * a.num_partitions;
         char *ws = reinterpret_cast<char *>(a.ws);
         kp.tickets = reinterpret_cast<unsigned *>(ws);
         ws += decode_ticket_bytes(a.B, a.Hkv);
@@ -1011,7 +1067,9 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
         kp.ws_acc = reinterpret_cast<float *>(ws + 2 * align256(n * sizeof(float)));
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
-    switch (G) {
+    kp.G = G;
+    kp.M = M;
+    switch (NCOL) {
     case 1: err = launch_split<1>(mk, mv, kp, grid, a.fused, stream); break;
     case 2: err = launch_split<2>(mk, mv, kp, grid, a.fused, stream); break;
     case 3: err = launch_split<3>(mk, mv, kp, grid, a.fused, stream); break;
@@ -1031,6 +1089,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     ma.B = a.B;
     ma.Hq = a.Hq;
     ma.NP = a.num_partitions;
+    ma.M = M;
     ma.out_f32 = a.out_f32;
     ma.out_bf16 = a.out_bf16;
     ma.context_lens = a.context_lens;
@@ -1050,16 +1109,41 @@ cudaError_t launch_merge(const MergeArgs &a, cudaStream_t stream)
     mp.acc = a.acc;
     mp.Hq = a.Hq;
     mp.NP = a.NP;
+    mp.M = a.M > 0 ? a.M : 1;
     mp.out_f32 = a.out_f32;
     mp.out_bf16 = reinterpret_cast<uint16_t *>(a.out_bf16);
     mp.context_lens = a.context_lens;
     mp.P = a.page_size;
     mp.ppp = a.pages_per_part;
     mp.max_pages = a.max_pages;
-    const unsigned rows = static_cast<unsigned>(a.B) * a.Hq;
+    const unsigned rows = static_cast<unsigned>(a.B) * mp.M * a.Hq;
     if (a.context_lens)
         return launch_pdl(merge_kernel<true>, dim3(rows), dim3(kMergeThreads), 0, stream, mp);
     return launch_pdl(merge_kernel<false>, dim3(rows), dim3(kMergeThreads), 0, stream, mp);
+}
+
+namespace {
+
+// One thread waits on an mbarrier that nothing completes: the bounded wait
+// gives up after kWaitLimitNs and raises the same flag as a copy that never
+// lands, so the failure path can be exercised without a fault.
+__global__ void wait_selftest_kernel()
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0)
+        return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0))
+        raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
+}
+
+} // namespace
+
+cudaError_t launch_wait_selftest(cudaStream_t stream)
+{
+    wait_selftest_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
 }
 
 cudaError_t read_flags_decode(unsigned *flags, bool clear)

@@ -19,6 +19,7 @@ struct PrologueArgs {
     int B, Hq, Hkv, page_size, max_pages, num_pages;
     double rope_theta;
     float eps;
+    int M; // new tokens per sequence, at positions T - M .. T - 1 (0 or 1: one)
 };
 
 struct DecodeArgs {
@@ -31,6 +32,7 @@ struct DecodeArgs {
     float *out_f32;      // nullable
     pgqa_bf16 *out_bf16; // nullable
     float *ws;           // partial states when NP > 1
+    int M; // new tokens (queries) per sequence; 0 or 1 = the single-token step
     // fused decode step (qk_norm_rope_append + attention in one launch)
     bool fused;
     const pgqa_bf16 *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
@@ -42,6 +44,7 @@ struct DecodeArgs {
 struct MergeArgs {
     const float *m, *l, *acc;
     int B, Hq, NP;
+    int M; // query rows per sequence are M * Hq (0 or 1: one)
     float *out_f32;
     pgqa_bf16 *out_bf16;
     // When context_lens is non-null, sequence b uses only its first
@@ -95,6 +98,7 @@ size_t decode_ticket_bytes(int B, int Hkv);
 // (and optionally clear) it synchronously on the current device.
 cudaError_t read_flags_prologue(unsigned *flags, bool clear);
 cudaError_t read_flags_decode(unsigned *flags, bool clear);
+cudaError_t launch_wait_selftest(cudaStream_t stream);
 
 // Launch `kernel` on `stream` with programmatic stream serialisation: it may
 // start while the previous kernel in the stream is still running, and must

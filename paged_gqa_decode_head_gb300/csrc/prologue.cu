@@ -28,7 +28,7 @@ struct PrologueParams {
     const uint16_t *q, *k, *v, *gamma_q, *gamma_k;
     const int32_t *context_lens, *block_table;
     uint16_t *k_cache, *v_cache, *q_out;
-    int B, Hq, Hkv, P, max_pages, num_pages;
+    int B, M, Hq, Hkv, P, max_pages, num_pages;
     float eps;
     RopeFreqs freqs;
 };
@@ -40,19 +40,22 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
     allow_dependent_launch();
     grid_dependency_wait();
     const int lane = threadIdx.x & 31;
+    // item = ((b * M + i) * (Hq + Hkv) + head): token i of sequence b sits at
+    // position T_b - M + i
     const int heads = p.Hq + p.Hkv;
     const int item = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    if (item >= p.B * heads)
+    if (item >= p.B * p.M * heads)
         return;
-    const int b = item / heads;
+    const int tok = item / heads; // b * M + i
+    const int b = tok / p.M;
     const int hh = item % heads;
     const int T = p.context_lens[b];
-    if (T < 1 || T > p.max_pages * p.P) {
-        if (hh == 0 && lane == 0)
+    if (T < p.M || T > p.max_pages * p.P) {
+        if (hh == 0 && tok % p.M == 0 && lane == 0)
             atomicOr(&g_flags_prologue, PGQA_DEVERR_BAD_CONTEXT);
         return;
     }
-    const int pos = T - 1;
+    const int pos = T - p.M + tok % p.M;
     const bool is_q = hh < p.Hq;
     const int h = is_q ? hh : hh - p.Hq;
 
@@ -60,9 +63,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
     const uint16_t *gamma;
     uint16_t *dst;
     if (is_q) {
-        src = p.q + (static_cast<size_t>(b) * p.Hq + h) * kHeadDim;
+        src = p.q + (static_cast<size_t>(tok) * p.Hq + h) * kHeadDim;
         gamma = p.gamma_q;
-        dst = p.q_out + (static_cast<size_t>(b) * p.Hq + h) * kHeadDim;
+        dst = p.q_out + (static_cast<size_t>(tok) * p.Hq + h) * kHeadDim;
     } else {
         const int phys = p.block_table[static_cast<size_t>(b) * p.max_pages + pos / p.P];
         if (phys < 0 || phys >= p.num_pages) {
@@ -71,11 +74,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
             return;
         }
         const size_t slot = ((static_cast<size_t>(phys) * p.Hkv + h) * p.P + pos % p.P) * kHeadDim;
-        src = p.k + (static_cast<size_t>(b) * p.Hkv + h) * kHeadDim;
+        src = p.k + (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim;
         gamma = p.gamma_k;
         dst = p.k_cache + slot;
         // V is appended bit for bit: 32 lanes x 8 bytes = one 256-byte row.
-        const uint2 *vrow = reinterpret_cast<const uint2 *>(p.v + (static_cast<size_t>(b) * p.Hkv + h) * kHeadDim);
+        const uint2 *vrow = reinterpret_cast<const uint2 *>(p.v + (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim);
         reinterpret_cast<uint2 *>(p.v_cache + slot)[lane] = vrow[lane];
     }
 
@@ -104,6 +107,7 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
     p.v_cache = a.v_cache;
     p.q_out = a.q_out;
     p.B = a.B;
+    p.M = a.M > 0 ? a.M : 1;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.P = a.page_size;
@@ -111,7 +115,7 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
     p.num_pages = a.num_pages;
     p.eps = a.eps;
     p.freqs = make_rope_freqs(a.rope_theta);
-    const long items = static_cast<long>(a.B) * (a.Hq + a.Hkv);
+    const long items = static_cast<long>(a.B) * p.M * (a.Hq + a.Hkv);
     const unsigned blocks = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
     return launch_pdl(prologue_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
 }

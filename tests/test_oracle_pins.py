@@ -376,3 +376,71 @@ def test_prologue_position_zero_is_plain_rmsnorm_and_norm_is_kept():
             x = oracle.bf16_widen(tok.q[0, 0])
             want = x / np.sqrt(np.mean(x * x) + 1e-6)
             assert np.max(np.abs(qo[0, 0] - want)) <= 2.0**-8 * np.max(np.abs(want))
+
+
+# --------------------------------------------------------------------------
+# multi-query decode: M new tokens, token i at position T - M + i, causal
+# --------------------------------------------------------------------------
+def _multi_case(seed, ctx, M, Hq=16, Hkv=8):
+    kv = inputs.paged_kv(seed, ctx, Hkv=Hkv, page_size=16)
+    q = inputs.normal_bf16(inputs.generator(seed, 91), (len(ctx), M, Hq, 128))
+    return kv, q
+
+
+def test_multi_attention_with_one_token_is_the_decode_step():
+    kv, q = _multi_case(700, [33, 200, 1], 1)
+    multi = oracle.decode_attention_multi(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, 0.09)
+    single = oracle.decode_attention(q[:, 0], kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, 0.09)
+    assert np.array_equal(multi[:, 0], single)
+
+
+@pytest.mark.parametrize("M", [2, 4, 7])
+def test_multi_attention_token_i_is_a_decode_at_its_own_prefix(M):
+    """Token i sees exactly the first T - M + i + 1 positions: the single-token
+    oracle with the context shortened by M - 1 - i gives the same row."""
+    kv, q = _multi_case(710 + M, [40, 17, 64], M)
+    multi = oracle.decode_attention_multi(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, 0.09)
+    for i in range(M):
+        ctx_i = kv.context_lens - (M - 1 - i)
+        single = oracle.decode_attention(q[:, i], kv.k_cache, kv.v_cache, kv.block_table, ctx_i, 0.09)
+        assert np.allclose(multi[:, i], single, rtol=0, atol=1e-13), i
+
+
+def test_multi_attention_first_token_of_a_fresh_sequence_returns_its_value():
+    """T = M: token 0 sees only position 0, so its output is V[0] exactly."""
+    M = 3
+    kv, q = _multi_case(720, [M, M], M)
+    multi = oracle.decode_attention_multi(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, 0.09)
+    for b in range(2):
+        page = kv.block_table[b, 0]
+        for h in range(16):
+            v0 = np.array([oracle.bf16_to_f64(x) for x in kv.v_cache[page, h // 2, 0]])
+            assert np.array_equal(multi[b, 0, h], v0)
+
+
+def test_multi_attention_refuses_context_shorter_than_m():
+    kv, q = _multi_case(730, [2, 30], 3)
+    with pytest.raises(oracle.OracleError):
+        oracle.decode_attention_multi(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, 0.09)
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_multi_prologue_equals_single_token_prologues_in_order(M):
+    """Token i of the multi prologue is the single-token prologue at context
+    length T - M + i + 1; applying those one after the other gives the same
+    rotated queries and the same cache bytes."""
+    ctx = [40, 17, 64]
+    kv = inputs.paged_kv(740 + M, ctx, Hkv=8, page_size=16)
+    g = inputs.generator(740 + M, 92)
+    q = inputs.normal_bf16(g, (3, M, 16, 128))
+    k = inputs.normal_bf16(g, (3, M, 8, 128))
+    v = inputs.normal_bf16(g, (3, M, 8, 128))
+    tok = inputs.new_token(740 + M, 3, 16, 8)
+    q_out, kc, vc = oracle.qk_norm_rope_append_multi(q, k, v, tok.gamma_q, tok.gamma_k, kv.context_lens,
+                                                     kv.block_table, kv.k_cache, kv.v_cache, 16, 1e6)
+    kc2, vc2 = kv.k_cache, kv.v_cache
+    for i in range(M):
+        qi, kc2, vc2 = oracle.qk_norm_rope_append(q[:, i], k[:, i], v[:, i], tok.gamma_q, tok.gamma_k,
+                                                  kv.context_lens - (M - 1 - i), kv.block_table, kc2, vc2, 16, 1e6)
+        assert np.array_equal(q_out[:, i], qi)
+    assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)

@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "ragged_b64", "long_split_kv_t128k", "host_tiled_t64k"],
+                    choices=[WORKLOAD, "ragged_b64", "long_split_kv_t128k", "host_tiled_t64k",
+                             "qwen3_0p6b_t8k_m4"],
                     help="the headline step (default) or one of the larger parity workloads, "
                          "measured on their own (one JSON line per variant, not the headline line)")
     ap.add_argument("--layers", type=int, default=None,
@@ -414,7 +415,7 @@ def run_secondary(args):
     w = inputs.WORKLOADS[args.workload]
     scale = 1.0 / math.sqrt(128)
     peak, peak_kind = load_peaks()
-    iters = max(3, min(args.steps, 50))
+    iters = max(3, min(args.steps, 500))
 
     def timed(fn):
         for _ in range(max(3, args.warmup)):
@@ -461,6 +462,60 @@ def run_secondary(args):
                  kv_bytes, s, peak, "GB/s", peak_kind,
                  {"config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "kv_bytes": kv_bytes,
                              "l2": "inputs larger than L2"}})
+        assert pg.device_error_flags() == 0
+        return
+
+    if args.workload == "qwen3_0p6b_t8k_m4":
+        # multi-token verification: per layer the M-token prologue and the
+        # M-token attention, 28 layers in one CUDA graph
+        layers = inputs.qwen3_layers_multi()
+        B, M, Hq, Hkv, T = w["B"], w["M"], w["Hq"], w["Hkv"], w["T"]
+        bufs = []
+        for kv, q, k, v, gq, gk in layers:
+            bufs.append(dict(kc=to_device_bf16(kv.k_cache, dev), vc=to_device_bf16(kv.v_cache, dev),
+                             bt=to_device_i32(kv.block_table, dev), ctx=to_device_i32(kv.context_lens, dev),
+                             q=to_device_bf16(q, dev), k=to_device_bf16(k, dev), v=to_device_bf16(v, dev),
+                             gq=to_device_bf16(gq, dev), gk=to_device_bf16(gk, dev),
+                             q_out=torch.empty((B, M, Hq, 128), dtype=torch.bfloat16, device=dev),
+                             out=torch.empty((B, M, Hq, 128), dtype=torch.float32, device=dev)))
+        P, max_pages = layers[0][0].page_size, layers[0][0].max_pages
+        n = pg.decode_attn_multi_workspace_size(B, M, Hq, Hkv, 128, P, max_pages, 0)
+        ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+
+        def two_launch():
+            for b_ in bufs:
+                pg.qk_norm_rope_append_multi(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                             b_["kc"], b_["vc"], b_["q_out"], w["theta"])
+                pg.decode_attn_paged_multi(b_["q_out"], b_["kc"], b_["vc"], b_["bt"], b_["ctx"], scale,
+                                           out_f32=b_["out"], workspace=ws)
+
+        def fused():
+            for b_ in bufs:
+                pg.decode_step_paged_multi(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                           b_["kc"], b_["vc"], scale, w["theta"], q_out=b_["q_out"],
+                                           out_f32=b_["out"], workspace=ws)
+
+        def capture(step):
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                step()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            return graph
+
+        L = len(layers)
+        kv_bytes = 4 * T * Hkv * 128 * L
+        for name, step in (("decode_step_paged_multi (one launch per layer)", fused),
+                           ("qk_norm_rope_append_multi + decode_attn_paged_multi", two_launch)):
+            s = timed(capture(step).replay)
+            emit(f"{name}, M={M}, {L} layers per graph", kv_bytes, s, peak, "GB/s", peak_kind,
+                 {"us_per_layer_step": s * 1e6 / L,
+                  "config": {"B": B, "M": M, "Hq": Hq, "Hkv": Hkv, "T": T, "P": P, "layers": L,
+                             "num_partitions": pg.decode_attn_partition_count(B, Hkv, P, max_pages, 0),
+                             "l2": "inputs larger than L2: 896 MiB of KV"}})
         assert pg.device_error_flags() == 0
         return
 

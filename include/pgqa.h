@@ -231,6 +231,22 @@ int qk_norm_rope_append_multi(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa
                               pgqa_bf16 *k_cache, pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int M,
                               int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
                               float rope_theta, float eps, cudaStream_t stream);
+/*
+ * decode_step_paged_multi -- qk_norm_rope_append_multi followed by
+ *   decode_attn_paged_multi in one launch (as decode_step_paged for M = 1):
+ *   q [B][M][Hq][D], k, v [B][M][Hkv][D], q_out (nullable) and outputs
+ *   [B][M][Hq][D], M * (Hq / Hkv) <= 8, T_b >= M; workspace as
+ *   decode_attn_multi_workspace_size. Each attention CTA rotates the (token,
+ *   head) queries it serves; the CTA whose range holds a new position appends
+ *   that token's K and V and requests the chunk holding it only afterwards.
+ */
+int decode_step_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                            const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                            const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
+                            pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int M, int Hq, int Hkv, int D,
+                            int page_size, int max_pages, int num_pages, float rope_theta, float eps,
+                            float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                            void *workspace, size_t ws_bytes, cudaStream_t stream);
 size_t decode_attn_multi_workspace_size(int B, int M, int Hq, int Hkv, int D, int page_size,
                                         int max_pages, int num_partitions);
 int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,

@@ -32,6 +32,7 @@ EXPORTED = (
     "qk_norm_rope_append_multi",
     "decode_attn_multi_workspace_size",
     "decode_attn_paged_multi",
+    "decode_step_paged_multi",
     "attn_partition_merge",
     "attn_tile_init",
     "attn_tile_update",
@@ -89,6 +90,8 @@ def load_library():
         lib.decode_attn_multi_workspace_size.restype = S
         lib.decode_attn_paged_multi.argtypes = [P] * 5 + [I] * 8 + [F, I, P, P, P, S, P]
         lib.decode_attn_paged_multi.restype = I
+        lib.decode_step_paged_multi.argtypes = [P] * 10 + [I] * 8 + [F, F, F, I, P, P, P, S, P]
+        lib.decode_step_paged_multi.restype = I
         lib.qk_norm_rope_append.restype = I
         lib.decode_attn_partition_count.argtypes = [I] * 5
         lib.decode_attn_partition_count.restype = I
@@ -251,6 +254,27 @@ def decode_attn_paged_multi(q, k_cache, v_cache, block_table, context_lens, scal
         _dev(out_f32, torch.float32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
         ws_ptr, ws_bytes, _stream(stream))
     _check("decode_attn_paged_multi", st)
+
+
+def decode_step_paged_multi(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache, scale: float,
+                            rope_theta: float, eps: float = 1e-6, q_out=None, out_f32=None, out_bf16=None,
+                            workspace=None, num_partitions: int = 0, stream=None) -> None:
+    """Fused multi-token step: q [B, M, Hq, D], k/v [B, M, Hkv, D], outputs [B, M, Hq, D]."""
+    lib = load_library()
+    bf, i32 = torch.bfloat16, torch.int32
+    B, M, Hq, D = q.shape
+    Hkv = k.shape[2]
+    num_pages, _, P, _ = k_cache.shape
+    ws_ptr = _dev(workspace, torch.uint8, "workspace", nullable=True)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.decode_step_paged_multi(
+        _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(gamma_q, bf, "gamma_q"),
+        _dev(gamma_k, bf, "gamma_k"), _dev(context_lens, i32, "context_lens"), _dev(block_table, i32, "block_table"),
+        _dev(k_cache, bf, "k_cache"), _dev(v_cache, bf, "v_cache"), _dev(q_out, bf, "q_out", nullable=True), B, M,
+        Hq, Hkv, D, P, block_table.shape[1], num_pages, float(rope_theta), float(eps), float(scale),
+        int(num_partitions), _dev(out_f32, torch.float32, "out_f32", nullable=True),
+        _dev(out_bf16, bf, "out_bf16", nullable=True), ws_ptr, ws_bytes, _stream(stream))
+    _check("decode_step_paged_multi", st)
 
 
 def decode_step_paged(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache, scale: float,

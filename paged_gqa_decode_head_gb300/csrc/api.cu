@@ -300,7 +300,7 @@ size_t decode_attn_multi_workspace_size(int B, int M, int Hq, int Hkv, int D, in
     return decode_attn_workspace_size(B, M * Hq, Hkv, D, page_size, max_pages, num_partitions);
 }
 
-int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+static int step_impl(const char *fn, int M, const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
                       const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
                       const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
                       pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D,
@@ -308,13 +308,17 @@ int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v
                       float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
                       void *workspace, size_t ws_bytes, cudaStream_t stream)
 {
-    const char *fn = "decode_step_paged";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
     if (int st = check_pages(fn, page_size, max_pages, num_pages))
         return st;
     if (num_partitions < 0)
         return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
+    if (M < 1)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: M = %d new tokens per sequence, need >= 1", fn, M);
+    if (M * (Hq / Hkv) > pgqa::kMaxGroupHost)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: M * (Hq / Hkv) = %d exceeds %d", fn, M * (Hq / Hkv),
+                    pgqa::kMaxGroupHost);
     if (!std::isfinite(scale))
         return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
     if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps))
@@ -336,7 +340,7 @@ int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, Hq, np);
+    const size_t need = pgqa::decode_workspace_bytes(B, Hkv, M * Hq, np);
     if (need > 0 && (!workspace || ws_bytes < need))
         return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu",
                     fn, need, np, workspace ? ws_bytes : static_cast<size_t>(0));
@@ -358,6 +362,7 @@ int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v
     a.out_bf16 = out_bf16;
     a.ws = static_cast<float *>(workspace);
     a.fused = true;
+    a.M = M;
     a.q_raw = q;
     a.k_new = k;
     a.v_new = v;
@@ -370,6 +375,32 @@ int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
     return ok();
+}
+
+int decode_step_paged(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                      const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                      const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
+                      pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D,
+                      int page_size, int max_pages, int num_pages, float rope_theta, float eps,
+                      float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                      void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    return step_impl("decode_step_paged", 1, q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache,
+                     v_cache, q_out, B, Hq, Hkv, D, page_size, max_pages, num_pages, rope_theta, eps, scale,
+                     num_partitions, out_f32, out_bf16, workspace, ws_bytes, stream);
+}
+
+int decode_step_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                            const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                            const int32_t *context_lens, const int32_t *block_table, pgqa_bf16 *k_cache,
+                            pgqa_bf16 *v_cache, pgqa_bf16 *q_out, int B, int M, int Hq, int Hkv, int D,
+                            int page_size, int max_pages, int num_pages, float rope_theta, float eps,
+                            float scale, int num_partitions, float *out_f32, pgqa_bf16 *out_bf16,
+                            void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    return step_impl("decode_step_paged_multi", M, q, k, v, gamma_q, gamma_k, context_lens, block_table,
+                     k_cache, v_cache, q_out, B, Hq, Hkv, D, page_size, max_pages, num_pages, rope_theta, eps,
+                     scale, num_partitions, out_f32, out_bf16, workspace, ws_bytes, stream);
 }
 
 int attn_partition_merge(const float *m, const float *l, const float *acc, int B, int Hq, int D,

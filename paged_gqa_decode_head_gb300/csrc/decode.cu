@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     // griddepcontrol.wait (the fused step patches its row into shared memory
     // itself instead).
     auto holds_new_token = [&](int k) {
-        return !kFused && chunk_token(k) + kChunkTokens > T - p.M;
+        return (!kFused || kMulti) && chunk_token(k) + kChunkTokens > T - p.M;
     };
     // Physical pages of this warp's chunks, 32 at a time: lane L caches the
     // entry of chunk 32*blk + L. Called by the whole (converged) warp.
@@ -523,39 +523,61 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 
     // fused step: what the prologue needs that no earlier kernel writes
     // (gains, rotation, the append slot) is prepared before the wait.
-    const int pos = T - 1;
-    const bool has_q = kFused && T > 0 && warp < NCOL; // fused: NCOL = G
-    int new_chunk = -1; // index k of the chunk holding pos in this warp's sequence, or -1
+    // Single token (kMulti = false): warps < G rotate the query heads; the
+    // warp owning the chunk of position T-1 computes the new K row, appends K
+    // and V and patches the row into its staged chunk. M tokens (kMulti):
+    // warp w < NCOL rotates column w (token w / G, head w % G) and warp w < M
+    // appends token w at T - M + w; chunks holding new positions are
+    // requested only once every append is done.
+    const bool has_q = kFused && T > 0 && warp < NCOL;
+    const int q_pos = kMulti ? T - p.M + warp / p.G : T - 1; // position of column `warp`
+    const bool has_tok = kFused && kMulti && T > 0 && warp < p.M;
+    const int tok_pos = T - p.M + warp; // kMulti: position of token `warp`
+    const int pos = T - 1;              // single token
+    int new_chunk = -1; // single token: index k of the chunk holding pos in this warp's sequence, or -1
     int new_phys = -1;
-    if (kFused && T > 0 && pos >= tok0 && pos < tok1) {
+    if (kFused && !kMulti && T > 0 && pos >= tok0 && pos < tok1) {
         const int c_idx = (pos - tok0) / kChunkTokens;
         if (c_idx % kWarps == warp) {
             new_chunk = c_idx / kWarps;
             new_phys = table[pos / p.P];
         }
     }
-    HeadRope rope;
+    if (has_tok) {
+        // token `warp`: its slot, appended by every partition's CTA that owns
+        // it -- the CTA whose range holds tok_pos
+        if (tok_pos >= tok0 && tok_pos < tok1)
+            new_phys = table[tok_pos / p.P];
+    }
+    const bool appends = kMulti ? (has_tok && tok_pos >= tok0 && tok_pos < tok1) : new_chunk >= 0;
+    HeadRope rope, rope_k;
     float gain_q[4], gain_k[4];
-    if (has_q || new_chunk >= 0)
-        rope.init(pos, p.freqs);
+    if (has_q)
+        rope.init(q_pos, p.freqs);
+    if (appends) {
+        if constexpr (kMulti)
+            rope_k.init(tok_pos, p.freqs);
+        else
+            rope_k = has_q ? rope : (rope.init(pos, p.freqs), rope);
+    }
     if (has_q)
         load_head(p.gamma_q, gain_q);
-    if (new_chunk >= 0)
+    if (appends)
         load_head(p.gamma_k, gain_k);
 
     grid_dependency_wait();
 
-    // The new token's q, k, v come from the previous kernels: load them now,
+    // The new tokens' q, k, v come from the previous kernels: load them now,
     // ahead of the remaining bulk requests.
-    const size_t qrow = (static_cast<size_t>(b) * p.Hq + kvh * NCOL + warp) * kHeadDim;
-    const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
+    const size_t qrow = has_q ? column_row<kMulti>(p, b, kvh, warp) * kHeadDim : 0;
+    const size_t krow = ((static_cast<size_t>(b) * (kMulti ? p.M : 1) + (kMulti ? warp : 0)) * p.Hkv + kvh) * kHeadDim;
     float xq[4], xk[4];
     uint16_t new_v[4] = {0, 0, 0, 0};
     MmaWarp<NCOL> st;
     const int col = lane >> 2; // this lane's B-operand column
     if (has_q)
         load_head(p.q_raw + qrow, xq);
-    if (new_chunk >= 0) {
+    if (appends) {
         load_head(p.k_new + krow, xk);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -563,16 +585,18 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     }
     if constexpr (!kFused)
         st.init(col < NCOL ? p.q + column_row<kMulti>(p, b, kvh, col) * kHeadDim : nullptr);
+    // the fused multi-token step requests new-token chunks after the appends
+    constexpr bool kDeferNew = kFused && kMulti;
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && (k >= kPrewaitChunks<kFused> || holds_new_token(k)))
+            if (k < first && (k >= kPrewaitChunks<kFused> || holds_new_token(k)) &&
+                !(kDeferNew && holds_new_token(k)))
                 issue(k, first_phys[k], policy);
     }
     __syncwarp();
 
-    // fused step: normalise and rotate q (warps < G) and the new K row (the
-    // warp owning its chunk), append K and V to the cache.
+    // fused step: normalise and rotate q and the new K rows, append K and V.
     uint16_t new_k[4] = {0, 0, 0, 0};
     if constexpr (kFused) {
         uint16_t *q_buf = reinterpret_cast<uint16_t *>(smem + kQBufOffset);
@@ -586,14 +610,15 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                     p.q_out[qrow + lane + 32 * i] = bits;
             }
         }
-        if (new_chunk >= 0) {
-            norm_rope_apply(xk, gain_k, p.eps, rope);
+        if (appends) {
+            norm_rope_apply(xk, gain_k, p.eps, rope_k);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 new_k[i] = f32_to_bf16_bits(xk[i]);
+            const int apos = kMulti ? tok_pos : pos;
             if (new_phys >= 0 && new_phys < p.num_pages) {
                 const size_t slot =
-                    ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + pos % p.P) * kHeadDim;
+                    ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + apos % p.P) * kHeadDim;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     p.k_cache[slot + lane + 32 * i] = new_k[i];
@@ -602,8 +627,19 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
             } else if (lane == 0) {
                 raise_flag(PGQA_DEVERR_BAD_PAGE);
             }
+            if constexpr (kDeferNew)
+                fence_proxy_async_global(); // the appends before the bulk reads of their chunks
         }
         __syncthreads();
+        if constexpr (kDeferNew) {
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < kStages; ++k)
+                    if (k < first && holds_new_token(k))
+                        issue(k, first_phys[k], policy);
+            }
+            __syncwarp();
+        }
         st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
     }
 
@@ -937,7 +973,8 @@ cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const Spl
                          dim3 grid, bool fused, cudaStream_t stream)
 {
     if (kp.M > 1)
-        return launch_split_t<NCOL, false, true>(mk, mv, kp, grid, stream);
+        return fused ? launch_split_t<NCOL, true, true>(mk, mv, kp, grid, stream)
+                     : launch_split_t<NCOL, false, true>(mk, mv, kp, grid, stream);
     return fused ? launch_split_t<NCOL, true, false>(mk, mv, kp, grid, stream)
                  : launch_split_t<NCOL, false, false>(mk, mv, kp, grid, stream);
 }

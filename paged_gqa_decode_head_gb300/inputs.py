@@ -198,6 +198,8 @@ WORKLOADS = {
     "long_split_kv_t128k": dict(seed=1003, B=1, Hq=32, Hkv=8, D=128, T=131072, page_size=16,
                                 partition=512, outlier_fraction=0.01, outlier_factor=8.0),
     "host_tiled_t64k": dict(seed=1004, B=1, Hq=16, Hkv=8, D=128, T=65536, tile=512),
+    "qwen3_0p6b_t8k_m4": dict(seed=1005, layers=28, B=1, M=4, Hq=16, Hkv=8, D=128, T=8192, page_size=16,
+                              theta=1e6),
 }
 
 
@@ -216,6 +218,25 @@ def qwen3_layers(layers: int | None = None, T: int | None = None):
                       fill_unused="normal")
         tok = new_token(seed, w["B"], w["Hq"], w["Hkv"], w["D"])
         out.append((kv, tok))
+    return out
+
+
+def qwen3_layers_multi(layers: int | None = None):
+    """Multi-token verification step: the Qwen3-0.6B-shaped 28-layer cache at
+    T = 8192 (T counting the M = 4 new tokens), per layer M new tokens
+    q [B,M,Hq,D], k, v [B,M,Hkv,D]. Returns [(PagedKV, q, k, v, gamma_q, gamma_k)]."""
+    w = WORKLOADS["qwen3_0p6b_t8k_m4"]
+    out = []
+    for i in range(w["layers"] if layers is None else layers):
+        seed = w["seed"] * 1000 + i
+        kv = paged_kv(seed, [w["T"]] * w["B"], Hkv=w["Hkv"], D=w["D"], page_size=w["page_size"], spare_pages=0,
+                      fill_unused="normal")
+        g = generator(seed, 60)
+        q = normal_bf16(g, (w["B"], w["M"], w["Hq"], w["D"]))
+        k = normal_bf16(g, (w["B"], w["M"], w["Hkv"], w["D"]))
+        v = normal_bf16(g, (w["B"], w["M"], w["Hkv"], w["D"]))
+        tok = new_token(seed, w["B"], w["Hq"], w["Hkv"], w["D"])
+        out.append((kv, q, k, v, tok.gamma_q, tok.gamma_k))
     return out
 
 

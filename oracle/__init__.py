@@ -63,6 +63,16 @@ def _load():
         lib.oracle_qk_norm_rope_append.argtypes = [P] * 10 + [I] * 7 + [D, D]
         lib.oracle_qk_norm_rope_append.restype = I
         lib.oracle_decode_attention.argtypes = [P] * 5 + [I] * 7 + [D, P]
+        lib.oracle_quantize_row_int8.argtypes = [P, I, P, P]
+        lib.oracle_quantize_row_int8.restype = None
+        lib.oracle_quantize_rows_int8.argtypes = [P, L, I, P, P]
+        lib.oracle_quantize_rows_int8.restype = None
+        lib.oracle_dequant_int8.argtypes = [ctypes.c_int8, ctypes.c_float]
+        lib.oracle_dequant_int8.restype = D
+        lib.oracle_qk_norm_rope_append_int8.argtypes = [P] * 12 + [I] * 7 + [D, D]
+        lib.oracle_qk_norm_rope_append_int8.restype = I
+        lib.oracle_decode_attention_int8.argtypes = [P] * 7 + [I] * 7 + [D, P]
+        lib.oracle_decode_attention_int8.restype = I
         lib.oracle_decode_attention_multi.argtypes = [P] * 5 + [I] * 8 + [D, P]
         lib.oracle_decode_attention_multi.restype = I
         lib.oracle_qk_norm_rope_append_multi.argtypes = [P] * 10 + [I] * 8 + [D, D]
@@ -249,6 +259,64 @@ def decode_attention_multi(q, k_cache, v_cache, block_table, context_lens, scale
     st = lib.oracle_decode_attention_multi(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(ctx), B, M, Hq, Hkv, D,
                                            P, bt.shape[1], num_pages, float(scale), _ptr(out))
     _check(st, "decode_attention_multi")
+    return out
+
+
+def quantize_rows_int8(rows):
+    """Symmetric per-row INT8 quantization of bf16 rows [..., D] (u16 bits).
+
+    Returns (codes int8 [..., D], scales float32 [...])."""
+    rows = _u16(rows)
+    D = rows.shape[-1]
+    n = rows.size // D
+    codes = np.zeros(rows.shape, dtype=np.int8)
+    scales = np.zeros(rows.shape[:-1], dtype=np.float32)
+    _load().oracle_quantize_rows_int8(_ptr(rows), n, D, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def dequantize_int8(codes, scales) -> np.ndarray:
+    """codes * scale per row, float64 (exact)."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def qk_norm_rope_append_int8(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache8, v_cache8, k_scale,
+                             v_scale, page_size: int, rope_theta: float, eps: float = 1e-6):
+    """Prologue with an INT8 cache. Returns (q_out, k_cache8', v_cache8', k_scale', v_scale') (copies)."""
+    lib = _load()
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    gq, gk = _u16(gamma_q), _u16(gamma_k)
+    ctx, bt = _i32(context_lens), _i32(block_table)
+    kc = np.ascontiguousarray(k_cache8, dtype=np.int8).copy()
+    vc = np.ascontiguousarray(v_cache8, dtype=np.int8).copy()
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32).copy()
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32).copy()
+    B, Hq, D = q.shape
+    Hkv = k.shape[1]
+    q_out = np.zeros_like(q)
+    st = lib.oracle_qk_norm_rope_append_int8(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gq), _ptr(gk), _ptr(ctx), _ptr(bt), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+        _ptr(q_out), B, Hq, Hkv, D, page_size, bt.shape[1], kc.shape[0], float(rope_theta), float(eps))
+    _check(st, "qk_norm_rope_append_int8")
+    return q_out, kc, vc, ks, vs
+
+
+def decode_attention_int8(q, k_cache8, v_cache8, k_scale, v_scale, block_table, context_lens,
+                          scale: float) -> np.ndarray:
+    """Direct-softmax decode attention over an INT8 cache (dequantized rows). float64 [B, Hq, D]."""
+    lib = _load()
+    q = _u16(q)
+    kc = np.ascontiguousarray(k_cache8, dtype=np.int8)
+    vc = np.ascontiguousarray(v_cache8, dtype=np.int8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt, ctx = _i32(block_table), _i32(context_lens)
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, _ = kc.shape
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    st = lib.oracle_decode_attention_int8(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(ctx), B,
+                                          Hq, Hkv, D, P, bt.shape[1], num_pages, float(scale), _ptr(out))
+    _check(st, "decode_attention_int8")
     return out
 
 

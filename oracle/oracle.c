@@ -294,6 +294,118 @@ int oracle_qk_norm_rope_append_multi(const uint16_t *q, const uint16_t *k, const
 }
 
 /* ------------------------------------------------------------------------- */
+/* INT8 KV rows [Qwen3 runtime s0.1: INT8 values times an FP32 scale,        */
+/*   accumulated in FP32; RTX 5090 residency page: int8 symmetric per-row     */
+/*   quantization halves the bytes a bandwidth-bound path moves]              */
+/* ------------------------------------------------------------------------- */
+
+/* Symmetric per-row quantization of one D-vector given as bf16 bits (a K row
+ * after RoPE and its bf16 rounding, or a V row as written):
+ *   amax = max_r |x_r|,  s = amax / 127,  code_r = round_half_even(x_r / s)
+ * (codes in [-127, 127]; an all-zero row has s = 0 and zero codes).
+ * Reading: the pages fix int8, symmetric, per row and an FP32 scale; the row
+ * here is one (position, KV head) vector. The scale and the quotients are
+ * formed in binary32 -- the precision in which the kernel takes the same
+ * integer decision -- with correctly rounded division. */
+void oracle_quantize_row_int8(const uint16_t *row, int D, int8_t *codes, float *scale)
+{
+    float amax = 0.0f;
+    for (int r = 0; r < D; ++r) {
+        float a = fabsf((float)oracle_bf16_to_double(row[r]));
+        if (a > amax)
+            amax = a;
+    }
+    volatile float s = amax / 127.0f; /* binary32, rounded once */
+    *scale = s;
+    for (int r = 0; r < D; ++r) {
+        if (amax == 0.0f) {
+            codes[r] = 0;
+            continue;
+        }
+        volatile float quot = (float)oracle_bf16_to_double(row[r]) / s;
+        float c = rintf(quot); /* round half to even (default rounding mode) */
+        if (c > 127.0f)
+            c = 127.0f;
+        if (c < -127.0f)
+            c = -127.0f;
+        codes[r] = (int8_t)c;
+    }
+}
+
+/* oracle_quantize_row_int8 applied to n consecutive rows of D values
+ * (a whole cache [num_pages][Hkv][P][D] -> codes of the same shape and one
+ * scale per row). */
+void oracle_quantize_rows_int8(const uint16_t *rows, long n, int D, int8_t *codes, float *scales)
+{
+    for (long i = 0; i < n; ++i)
+        oracle_quantize_row_int8(rows + i * D, D, codes + i * D, scales + i);
+}
+
+/* Dequantized value code * scale, exact in double. */
+double oracle_dequant_int8(int8_t code, float scale) { return (double)code * (double)scale; }
+
+/* The prologue with an INT8 cache: as oracle_qk_norm_rope_append, except that
+ * the K slot receives the int8 codes and the scale of the bf16-rounded
+ * rotated K row, and the V slot those of the V row. Caches are int8
+ * [num_pages][Hkv][P][D], scales float [num_pages][Hkv][P]. */
+int oracle_qk_norm_rope_append_int8(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                    const uint16_t *gamma_q, const uint16_t *gamma_k,
+                                    const int32_t *context_lens, const int32_t *block_table,
+                                    int8_t *k_cache, int8_t *v_cache, float *k_scale,
+                                    float *v_scale, uint16_t *q_out, int B, int Hq, int Hkv, int D,
+                                    int P, int max_pages, int num_pages, double theta, double eps)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || (D % 2) != 0 || P <= 0 || Hq % Hkv != 0)
+        return ORACLE_BAD_ARG;
+    double *x = malloc(sizeof(double) * (size_t)D * 4);
+    uint16_t *kb = malloc(sizeof(uint16_t) * (size_t)D);
+    if (!x || !kb) {
+        free(x), free(kb);
+        return ORACLE_NO_MEMORY;
+    }
+    double *gam = x + D, *nrm = x + 2 * D, *rot = x + 3 * D;
+    int status = ORACLE_OK;
+    for (int b = 0; b < B && status == ORACLE_OK; ++b) {
+        long T = context_lens[b];
+        if (T < 1 || T > (long)max_pages * P) {
+            status = ORACLE_BAD_ARG;
+            break;
+        }
+        long pos = T - 1;
+        for (int h = 0; h < Hq; ++h) {
+            for (int r = 0; r < D; ++r) {
+                x[r] = oracle_bf16_to_double(q[((long)b * Hq + h) * D + r]);
+                gam[r] = oracle_bf16_to_double(gamma_q[r]);
+            }
+            oracle_head_rmsnorm(x, gam, D, eps, nrm);
+            oracle_rope_half(nrm, D, pos, theta, rot);
+            for (int r = 0; r < D; ++r)
+                q_out[((long)b * Hq + h) * D + r] = oracle_round_bf16(rot[r]);
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            long off = oracle_cache_offset(block_table, max_pages, num_pages, b, h, pos, Hkv, P, D);
+            if (off < 0) {
+                status = ORACLE_BAD_ARG;
+                break;
+            }
+            for (int r = 0; r < D; ++r) {
+                x[r] = oracle_bf16_to_double(k[((long)b * Hkv + h) * D + r]);
+                gam[r] = oracle_bf16_to_double(gamma_k[r]);
+            }
+            oracle_head_rmsnorm(x, gam, D, eps, nrm);
+            oracle_rope_half(nrm, D, pos, theta, rot);
+            for (int r = 0; r < D; ++r)
+                kb[r] = oracle_round_bf16(rot[r]);
+            long row = off / D; /* (page, head, slot) index of the scale arrays */
+            oracle_quantize_row_int8(kb, D, k_cache + off, k_scale + row);
+            oracle_quantize_row_int8(v + ((long)b * Hkv + h) * D, D, v_cache + off, v_scale + row);
+        }
+    }
+    free(x), free(kb);
+    return status;
+}
+
+/* ------------------------------------------------------------------------- */
 /* A5 + A6: decode attention, full softmax [Qwen3 runtime s2.5, s2.6]        */
 /* ------------------------------------------------------------------------- */
 
@@ -443,6 +555,61 @@ int oracle_decode_attention_multi(const uint16_t *q, const uint16_t *k_cache,
                 long visible = T - M + i + 1; /* positions 0 .. t_i */
                 softmax_attend(qv, keys, values, visible, D, scale, scores, out + row * D);
             }
+        }
+    }
+    free(keys), free(values), free(scores), free(qv);
+    return status;
+}
+
+/* Decode attention over an INT8 cache: oracle_decode_attention with every
+ * key and value row replaced by its dequantized values code * scale. */
+int oracle_decode_attention_int8(const uint16_t *q, const int8_t *k_cache, const int8_t *v_cache,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *block_table, const int32_t *context_lens, int B,
+                                 int Hq, int Hkv, int D, int P, int max_pages, int num_pages,
+                                 double scale, double *out)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv != 0)
+        return ORACLE_BAD_ARG;
+    long Tmax = 0;
+    for (int b = 0; b < B; ++b) {
+        if (context_lens[b] < 0 || (long)context_lens[b] > (long)max_pages * P)
+            return ORACLE_BAD_ARG;
+        if (context_lens[b] > Tmax)
+            Tmax = context_lens[b];
+    }
+    size_t n = (size_t)(Tmax > 0 ? Tmax : 1);
+    double *keys = malloc(sizeof(double) * n * (size_t)D);
+    double *values = malloc(sizeof(double) * n * (size_t)D);
+    double *scores = malloc(sizeof(double) * n);
+    double *qv = malloc(sizeof(double) * (size_t)D);
+    if (!keys || !values || !scores || !qv) {
+        free(keys), free(values), free(scores), free(qv);
+        return ORACLE_NO_MEMORY;
+    }
+    int status = ORACLE_OK;
+    for (int b = 0; b < B && status == ORACLE_OK; ++b) {
+        long T = context_lens[b];
+        for (int h = 0; h < Hq && status == ORACLE_OK; ++h) {
+            int kvh = oracle_kv_head(h, Hq, Hkv);
+            for (long j = 0; j < T; ++j) {
+                long off = oracle_cache_offset(block_table, max_pages, num_pages, b, kvh, j, Hkv,
+                                               P, D);
+                if (off < 0) {
+                    status = ORACLE_BAD_ARG;
+                    break;
+                }
+                long row = off / D;
+                for (int r = 0; r < D; ++r) {
+                    keys[j * D + r] = oracle_dequant_int8(k_cache[off + r], k_scale[row]);
+                    values[j * D + r] = oracle_dequant_int8(v_cache[off + r], v_scale[row]);
+                }
+            }
+            if (status != ORACLE_OK)
+                break;
+            for (int r = 0; r < D; ++r)
+                qv[r] = oracle_bf16_to_double(q[((long)b * Hq + h) * D + r]);
+            softmax_attend(qv, keys, values, T, D, scale, scores, out + ((long)b * Hq + h) * D);
         }
     }
     free(keys), free(values), free(scores), free(qv);

@@ -444,3 +444,80 @@ def test_multi_prologue_equals_single_token_prologues_in_order(M):
                                                   kv.context_lens - (M - 1 - i), kv.block_table, kc2, vc2, 16, 1e6)
         assert np.array_equal(q_out[:, i], qi)
     assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)
+
+
+# --------------------------------------------------------------------------
+# INT8 KV rows: symmetric per-row quantization with an FP32 scale
+# (Qwen3 runtime s0.1; RTX 5090 residency page, int8 note)
+# --------------------------------------------------------------------------
+def _bits(values) -> np.ndarray:
+    t = torch.tensor(np.asarray(values, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_int8_row_amax_maps_to_127_and_error_is_half_a_step():
+    rows = inputs.normal_bf16(inputs.generator(600, 1), (64, 128))
+    codes, scales = oracle.quantize_rows_int8(rows)
+    x = oracle.bf16_to_f64(rows)
+    amax = np.abs(x).max(axis=1)
+    assert np.allclose(scales, (amax / 127).astype(np.float32), rtol=0, atol=0)
+    assert np.all(np.abs(codes).max(axis=1) == 127)
+    err = np.abs(x - oracle.dequantize_int8(codes, scales))
+    # half a step, plus the binary32 rounding of x / s (|x / s| <= 127, 2^-24 relative)
+    assert np.all(err <= scales[:, None] * (0.5 + 127 * 2.0 ** -23))
+
+
+def test_int8_row_ties_round_to_even_and_sign_is_symmetric():
+    # amax = 127 makes the scale exactly 1, so x / s = x
+    row = _bits([127.0, 2.5, 3.5, -2.5, -3.5, 0.5, 1.5, -126.5] + [0.0] * 120)
+    codes, scales = oracle.quantize_rows_int8(row[None])
+    assert scales[0] == 1.0
+    assert list(codes[0, :8]) == [127, 2, 4, -2, -4, 0, 2, -126]
+    neg = _bits(-oracle.bf16_to_f64(row))
+    codes_n, scales_n = oracle.quantize_rows_int8(neg[None])
+    assert scales_n[0] == scales[0] and np.array_equal(codes_n, -codes)
+
+
+def test_int8_zero_row_has_zero_scale_and_codes():
+    codes, scales = oracle.quantize_rows_int8(np.zeros((1, 128), dtype=np.uint16))
+    assert scales[0] == 0.0 and not codes.any()
+
+
+def test_int8_attention_equals_bf16_attention_when_dequantized_values_are_bf16():
+    """With power-of-two scales every code * scale is a bf16 value (|code| <=
+    127 < 256), so the INT8 attention must equal the bf16 oracle on that
+    dequantized cache exactly."""
+    kv = inputs.paged_kv(610, [40, 17, 3], Hkv=8, page_size=16, fill_unused="normal")
+    g = np.random.default_rng(611)
+    k8 = g.integers(-127, 128, kv.k_cache.shape, dtype=np.int8)
+    v8 = g.integers(-127, 128, kv.v_cache.shape, dtype=np.int8)
+    ks = (2.0 ** g.integers(-9, -4, kv.k_cache.shape[:-1])).astype(np.float32)
+    vs = (2.0 ** g.integers(-9, -4, kv.v_cache.shape[:-1])).astype(np.float32)
+    kb = _bits(oracle.dequantize_int8(k8, ks))
+    vb = _bits(oracle.dequantize_int8(v8, vs))
+    assert np.array_equal(oracle.bf16_to_f64(kb), oracle.dequantize_int8(k8, ks))  # exactly representable
+    q = inputs.query(610, 3, 16)
+    got = oracle.decode_attention_int8(q, k8, v8, ks, vs, kv.block_table, kv.context_lens, 0.09)
+    ref = oracle.decode_attention(q, kb, vb, kv.block_table, kv.context_lens, 0.09)
+    assert np.array_equal(got, ref)
+
+
+def test_int8_prologue_quantizes_the_bf16_prologue_rows():
+    """The INT8 prologue's K and V slots hold the per-row quantization of the
+    bf16 prologue's K slot and of the V row; q_out is the same."""
+    ctx = [40, 17, 64]
+    kv = inputs.paged_kv(620, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    tok = inputs.new_token(620, 3, 16, 8)
+    k8, ks = oracle.quantize_rows_int8(kv.k_cache)
+    v8, vs = oracle.quantize_rows_int8(kv.v_cache)
+    q_out, kc8, vc8, ks2, vs2 = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, 1e6)
+    q_ref, kc_ref, vc_ref = oracle.qk_norm_rope_append(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                       kv.context_lens, kv.block_table, kv.k_cache, kv.v_cache,
+                                                       16, 1e6)
+    assert np.array_equal(q_out, q_ref)
+    k8_ref, ks_ref = oracle.quantize_rows_int8(kc_ref)
+    v8_ref, vs_ref = oracle.quantize_rows_int8(vc_ref)
+    assert np.array_equal(kc8, k8_ref) and np.array_equal(ks2, ks_ref)
+    assert np.array_equal(vc8, v8_ref) and np.array_equal(vs2, vs_ref)

@@ -256,6 +256,43 @@ int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const 
                             void *workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * INT8 KV cache (the quantization scheme of "From Qwen3 math to CUDA
+ * kernels", s0.1 -- INT8 values times an FP32 scale, accumulated in FP32 --
+ * and of the RTX 5090 residency page's int8 note: symmetric, per row; on a
+ * bandwidth-bound path halving the bytes halves the time). Each (position,
+ * KV head) row of K and of V is stored as 128 int8 codes and one float scale:
+ *   s = amax_r |x_r| / 127,  code_r = round_half_even(x_r / s)  (binary32,
+ *   correctly rounded division; an all-zero row has s = 0),
+ * and read back as code * s. K is quantized after RoPE and its bf16 rounding,
+ * V as written. A row costs 2 x 128 + 8 bytes instead of 512.
+ *
+ *   k_cache8, v_cache8  int8 [num_pages][Hkv][page_size][D] (layout as the
+ *                       bf16 cache), 16-byte aligned
+ *   k_scale, v_scale    float [num_pages][Hkv][page_size], 16-byte aligned
+ *
+ * qk_norm_rope_append_int8 -- qk_norm_rope_append writing the new token's K
+ *   and V rows into the INT8 cache (codes and scales); q_out as before.
+ * decode_attn_paged_int8 -- decode_attn_paged over the INT8 cache: the same
+ *   attention with every key and value row dequantized. The query must lie
+ *   in the fp16 range (|q| < 65504; the fold runs fp16 tensor-core MMAs).
+ *   Reading and PDL rules as decode_attn_paged; workspace of
+ *   decode_attn_int8_workspace_size bytes (no initial value needed).
+ */
+int qk_norm_rope_append_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                             const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                             const int32_t *context_lens, const int32_t *block_table, int8_t *k_cache8,
+                             int8_t *v_cache8, float *k_scale, float *v_scale, pgqa_bf16 *q_out, int B,
+                             int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                             float rope_theta, float eps, cudaStream_t stream);
+size_t decode_attn_int8_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                       int num_partitions);
+int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int8_t *v_cache8,
+                           const float *k_scale, const float *v_scale, const int32_t *block_table,
+                           const int32_t *context_lens, int B, int Hq, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages, float scale, int num_partitions, float *out_f32,
+                           pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * attn_partition_merge -- exact merge of NP partition states (s9.1).
  *   m, l  [B][Hq][NP] float   running max of the scores (natural-log units)
  *                             and the softmax denominator, both relative to m

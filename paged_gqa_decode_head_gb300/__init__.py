@@ -15,8 +15,10 @@ from .binding import (  # noqa: F401
     attn_tile_finalize,
     attn_tile_init,
     attn_tile_update,
+    decode_attn_int8_workspace_size,
     decode_attn_multi_workspace_size,
     decode_attn_paged,
+    decode_attn_paged_int8,
     decode_attn_paged_multi,
     decode_attn_paged_static,
     decode_step_paged,
@@ -27,5 +29,6 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
     qk_norm_rope_append,
+    qk_norm_rope_append_int8,
     qk_norm_rope_append_multi,
 )

@@ -115,12 +115,14 @@ int pgqa_device_error(unsigned *flags_out, int clear)
     cudaError_t err = cudaDeviceSynchronize();
     if (err != cudaSuccess)
         return cuda_fail(err, "pgqa_device_error");
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     if ((err = pgqa::read_flags_prologue(&a, clear != 0)) != cudaSuccess)
         return cuda_fail(err, "pgqa_device_error");
     if ((err = pgqa::read_flags_decode(&b, clear != 0)) != cudaSuccess)
         return cuda_fail(err, "pgqa_device_error");
-    *flags_out = a | b;
+    if ((err = pgqa::read_flags_int8(&c, clear != 0)) != cudaSuccess)
+        return cuda_fail(err, "pgqa_device_error");
+    *flags_out = a | b | c;
     return ok();
 }
 
@@ -648,6 +650,128 @@ int attn_host_direct(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf1
     a.out_bf16 = out_bf16;
     a.ws = static_cast<float *>(workspace);
     cudaError_t err = pgqa::launch_host_direct(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+
+int qk_norm_rope_append_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                             const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                             const int32_t *context_lens, const int32_t *block_table, int8_t *k_cache8,
+                             int8_t *v_cache8, float *k_scale, float *v_scale, pgqa_bf16 *q_out, int B,
+                             int Hq, int Hkv, int D, int page_size, int max_pages, int num_pages,
+                             float rope_theta, float eps, cudaStream_t stream)
+{
+    const char *fn = "qk_norm_rope_append_int8";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (int st = check_pages(fn, page_size, max_pages, num_pages))
+        return st;
+    if (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: rope_theta must be > 0 and eps >= 0", fn);
+    if (B == 0)
+        return ok();
+    if (!q || !k || !v || !gamma_q || !gamma_k || !context_lens || !block_table || !k_cache8 || !v_cache8 ||
+        !k_scale || !v_scale || !q_out)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(gamma_q) || !aligned16(gamma_k) ||
+        !aligned16(k_cache8) || !aligned16(v_cache8) || !aligned16(k_scale) || !aligned16(v_scale) ||
+        !aligned16(q_out) || !aligned4(context_lens) || !aligned4(block_table))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
+    pgqa::PrologueArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.gamma_q = gamma_q;
+    a.gamma_k = gamma_k;
+    a.context_lens = context_lens;
+    a.block_table = block_table;
+    a.q_out = q_out;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.rope_theta = static_cast<double>(rope_theta);
+    a.eps = eps;
+    a.M = 1;
+    a.k_cache8 = k_cache8;
+    a.v_cache8 = v_cache8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    cudaError_t err = pgqa::launch_prologue(a, stream);
+    if (err != cudaSuccess)
+        return cuda_fail(err, fn);
+    return ok();
+}
+
+size_t decode_attn_int8_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                       int num_partitions)
+{
+    (void)D;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || page_size <= 0 || max_pages < 0 || num_partitions < 0)
+        return 0;
+    const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                           sm_count_current_device());
+    return pgqa::decode_int8_workspace_bytes(B, Hq, np);
+}
+
+int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int8_t *v_cache8,
+                           const float *k_scale, const float *v_scale, const int32_t *block_table,
+                           const int32_t *context_lens, int B, int Hq, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages, float scale, int num_partitions, float *out_f32,
+                           pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    const char *fn = "decode_attn_paged_int8";
+    if (int st = check_heads(fn, B, Hq, Hkv, D))
+        return st;
+    if (int st = check_pages(fn, page_size, max_pages, num_pages))
+        return st;
+    if (num_partitions < 0)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
+    if (!std::isfinite(scale))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (static_cast<long long>(num_pages) * Hkv * page_size > 0x7FFFFFFFLL)
+        return fail(PGQA_ERR_UNSUPPORTED, "%s: num_pages * Hkv * page_size exceeds 2^31 - 1 rows", fn);
+    if (B == 0)
+        return ok();
+    if (!q || !k_cache8 || !v_cache8 || !k_scale || !v_scale || !block_table || !context_lens)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
+    if (!out_f32 && !out_bf16)
+        return fail(PGQA_ERR_INVALID_ARG, "%s: out_f32 and out_bf16 are both NULL", fn);
+    if (!aligned16(q) || !aligned16(k_cache8) || !aligned16(v_cache8) || !aligned16(k_scale) ||
+        !aligned16(v_scale) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) ||
+        !aligned4(block_table) || !aligned4(context_lens) || (workspace && !aligned16(workspace)))
+        return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
+    const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
+                                           sm_count_current_device());
+    const size_t need = pgqa::decode_int8_workspace_bytes(B, Hq, np);
+    if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu", fn, need,
+                    np, workspace ? ws_bytes : static_cast<size_t>(0));
+    pgqa::DecodeInt8Args a{};
+    a.q = q;
+    a.k_cache8 = k_cache8;
+    a.v_cache8 = v_cache8;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.context_lens = context_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.page_size = page_size;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.num_partitions = np;
+    a.pages_per_part = max_pages > 0 ? (max_pages + np - 1) / np : 1;
+    a.out_f32 = out_f32;
+    a.out_bf16 = out_bf16;
+    a.ws = static_cast<float *>(workspace);
+    cudaError_t err = pgqa::launch_decode_int8(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
     return ok();

@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "pgqa.h"
@@ -242,6 +243,46 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
                  "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// As mma_bf16_16816 with fp16 A and B operands.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two int8 bytes of `bytes` (selected by `sel`: byte index of the low half
+// in bits 0-3, of the high half in bits 8-11) -> fp16x2, exactly: the biased
+// byte b + 128 becomes the mantissa of 1024 (fp16 0x6400 | byte), and 1152 is
+// subtracted.
+__device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t bytes, uint32_t sel)
+{
+    const uint32_t biased = bytes ^ 0x80808080u;
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel | 0x4040u);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// Two floats -> packed fp16x2 (nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t pair)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(pair & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t pair)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(pair >> 16)));
 }
 
 // Transpose an 8x8 b16 matrix held as an mma fragment (thread (g, t) holds

@@ -20,6 +20,9 @@ struct PrologueArgs {
     double rope_theta;
     float eps;
     int M; // new tokens per sequence, at positions T - M .. T - 1 (0 or 1: one)
+    // INT8 cache instead of k_cache / v_cache when k_cache8 is set
+    int8_t *k_cache8, *v_cache8;
+    float *k_scale, *v_scale;
 };
 
 struct DecodeArgs {
@@ -99,6 +102,23 @@ size_t decode_ticket_bytes(int B, int Hkv);
 cudaError_t read_flags_prologue(unsigned *flags, bool clear);
 cudaError_t read_flags_decode(unsigned *flags, bool clear);
 cudaError_t launch_wait_selftest(cudaStream_t stream);
+
+// Decode attention over an INT8 cache (decode_int8.cu).
+struct DecodeInt8Args {
+    const pgqa_bf16 *q;
+    const int8_t *k_cache8, *v_cache8;
+    const float *k_scale, *v_scale;
+    const int32_t *block_table, *context_lens;
+    int B, Hq, Hkv, page_size, max_pages, num_pages;
+    float scale;
+    int num_partitions, pages_per_part;
+    float *out_f32;
+    pgqa_bf16 *out_bf16;
+    float *ws;
+};
+cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream);
+size_t decode_int8_workspace_bytes(int B, int Hq, int num_partitions);
+cudaError_t read_flags_int8(unsigned *flags, bool clear);
 
 // Launch `kernel` on `stream` with programmatic stream serialisation: it may
 // start while the previous kernel in the stream is still running, and must

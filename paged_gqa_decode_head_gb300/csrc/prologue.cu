@@ -28,11 +28,37 @@ struct PrologueParams {
     const uint16_t *q, *k, *v, *gamma_q, *gamma_k;
     const int32_t *context_lens, *block_table;
     uint16_t *k_cache, *v_cache, *q_out;
+    // INT8 cache (kInt8): codes [num_pages][Hkv][P][D] and one FP32 scale per row
+    int8_t *k_cache8, *v_cache8;
+    float *k_scale, *v_scale;
     int B, M, Hq, Hkv, P, max_pages, num_pages;
     float eps;
     RopeFreqs freqs;
 };
 
+// Symmetric per-row INT8 quantization of the head held by the warp (x[i] is
+// dim lane + 32 i): s = amax / 127, code = round_half_even(x / s), both in
+// binary32 with correctly rounded division (an all-zero row: s = 0, codes 0).
+__device__ __forceinline__ void store_row_int8(const float (&x)[4], int8_t *codes, float *scale)
+{
+    const int lane = threadIdx.x & 31;
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int c = 0;
+        if (amax > 0.0f)
+            c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], s))));
+        codes[lane + 32 * i] = static_cast<int8_t>(c);
+    }
+    if (lane == 0)
+        *scale = s;
+}
+
+template <bool kInt8>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
 {
     // Everything this kernel reads may come from the kernel before it, and
@@ -61,7 +87,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
 
     const uint16_t *src;
     const uint16_t *gamma;
-    uint16_t *dst;
+    uint16_t *dst = nullptr;
+    size_t slot = 0;
     if (is_q) {
         src = p.q + (static_cast<size_t>(tok) * p.Hq + h) * kHeadDim;
         gamma = p.gamma_q;
@@ -73,17 +100,33 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
                 atomicOr(&g_flags_prologue, PGQA_DEVERR_BAD_PAGE);
             return;
         }
-        const size_t slot = ((static_cast<size_t>(phys) * p.Hkv + h) * p.P + pos % p.P) * kHeadDim;
+        slot = ((static_cast<size_t>(phys) * p.Hkv + h) * p.P + pos % p.P) * kHeadDim;
         src = p.k + (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim;
         gamma = p.gamma_k;
-        dst = p.k_cache + slot;
-        // V is appended bit for bit: 32 lanes x 8 bytes = one 256-byte row.
-        const uint2 *vrow = reinterpret_cast<const uint2 *>(p.v + (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim);
-        reinterpret_cast<uint2 *>(p.v_cache + slot)[lane] = vrow[lane];
+        const uint16_t *vsrc = p.v + (static_cast<size_t>(tok) * p.Hkv + h) * kHeadDim;
+        if constexpr (kInt8) {
+            float xv[4];
+            load_head(vsrc, xv);
+            store_row_int8(xv, p.v_cache8 + slot, p.v_scale + slot / kHeadDim);
+        } else {
+            dst = p.k_cache + slot;
+            // V is appended bit for bit: 32 lanes x 8 bytes = one 256-byte row.
+            const uint2 *vrow = reinterpret_cast<const uint2 *>(vsrc);
+            reinterpret_cast<uint2 *>(p.v_cache + slot)[lane] = vrow[lane];
+        }
     }
 
     float x[4];
     norm_rope_head(src, gamma, p.eps, pos, p.freqs, x);
+    if (kInt8 && !is_q) {
+        // quantize the bf16-rounded rotated K row
+        float xb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            xb[i] = bf16_bits_to_f32(f32_to_bf16_bits(x[i]));
+        store_row_int8(xb, p.k_cache8 + slot, p.k_scale + slot / kHeadDim);
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         dst[lane + 32 * i] = f32_to_bf16_bits(x[i]);
@@ -115,9 +158,15 @@ cudaError_t launch_prologue(const PrologueArgs &a, cudaStream_t stream)
     p.num_pages = a.num_pages;
     p.eps = a.eps;
     p.freqs = make_rope_freqs(a.rope_theta);
+    p.k_cache8 = a.k_cache8;
+    p.v_cache8 = a.v_cache8;
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
     const long items = static_cast<long>(a.B) * p.M * (a.Hq + a.Hkv);
     const unsigned blocks = static_cast<unsigned>((items + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    return launch_pdl(prologue_kernel, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
+    if (a.k_cache8)
+        return launch_pdl(prologue_kernel<true>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
+    return launch_pdl(prologue_kernel<false>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, stream, p);
 }
 
 cudaError_t read_flags_prologue(unsigned *flags, bool clear)

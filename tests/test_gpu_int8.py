@@ -1,0 +1,187 @@
+"""GPU parity of the INT8 KV cache: qk_norm_rope_append_int8 and
+decode_attn_paged_int8 against the oracle's INT8 definitions, and a quality
+gate of INT8 attention against bf16 attention on the same history."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_head_gb300 as pg
+from paged_gqa_decode_head_gb300 import binding, inputs
+from paged_gqa_decode_head_gb300.runner import bf16_bits, to_device_bf16, to_device_i32
+from parity_util import assert_bf16_close
+
+pytestmark = pytest.mark.gpu
+
+ATOL_F32 = 2e-3
+SCALE = 1.0 / math.sqrt(128)
+THETA = 1e6
+
+
+@pytest.fixture(autouse=True)
+def _clean_flags():
+    pg.device_error_flags(clear=True)
+    yield
+
+
+def int8_cache(kv):
+    """The oracle's INT8 quantization of a bf16 paged cache; scales of slots
+    past each sequence's end are set to NaN (the kernel must never use them)."""
+    k8, ks = oracle.quantize_rows_int8(kv.k_cache)
+    v8, vs = oracle.quantize_rows_int8(kv.v_cache)
+    P = kv.page_size
+    for b, T in enumerate(kv.context_lens):
+        if T % P:
+            page = kv.block_table[b, T // P]
+            if 0 <= page < kv.num_pages:
+                ks[page, :, T % P:] = np.nan
+                vs[page, :, T % P:] = np.nan
+    return k8, v8, ks, vs
+
+
+def dev_i8(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int8)).cuda()
+
+
+def dev_f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def run_attention(kv, q, k8, v8, ks, vs, num_partitions=0):
+    B, Hq, _ = q.shape
+    Hkv = kv.k_cache.shape[1]
+    n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, num_partitions)
+    ws = torch.zeros(max(16, n), dtype=torch.uint8, device="cuda")
+    of = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+    ob = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pg.decode_attn_paged_int8(to_device_bf16(q, "cuda"), dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs),
+                              to_device_i32(kv.block_table, "cuda"), to_device_i32(kv.context_lens, "cuda"), SCALE,
+                              out_f32=of, out_bf16=ob, workspace=ws, num_partitions=num_partitions)
+    torch.cuda.synchronize()
+    return of.cpu().numpy(), bf16_bits(ob)
+
+
+def check_attention(kv, q, num_partitions=0):
+    k8, v8, ks, vs = int8_cache(kv)
+    of, ob = run_attention(kv, q, k8, v8, ks, vs, num_partitions)
+    ref = oracle.decode_attention_int8(q, k8, v8, ks, vs, kv.block_table, kv.context_lens, SCALE)
+    assert np.isfinite(of).all()
+    assert np.abs(of - ref).max() <= ATOL_F32
+    assert_bf16_close(ob, oracle.round_bf16(ref), "out_bf16")
+    assert pg.device_error_flags() == 0
+    return of
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 33, 513, 1000])
+def test_int8_attention_small_contexts(T):
+    kv = inputs.paged_kv(1100 + T, [T, T + 5], Hkv=8, page_size=16, fill_unused="normal")
+    check_attention(kv, inputs.query(1100 + T, 2, 16))
+
+
+@pytest.mark.parametrize("num_partitions", [0, 1, 3, 70])
+def test_int8_attention_ragged_and_partitions(num_partitions):
+    ctx = [1, 17, 300, 4097, 2000]
+    kv = inputs.paged_kv(1120 + num_partitions, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    check_attention(kv, inputs.query(1120, len(ctx), 16), num_partitions)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (24, 8), (32, 8), (64, 8), (4, 1)])
+def test_int8_attention_group_sizes(Hq, Hkv):
+    kv = inputs.paged_kv(1140 + Hq, [700, 33], Hkv=Hkv, page_size=16, fill_unused="normal")
+    check_attention(kv, inputs.query(1140 + Hq, 2, Hq), 0)
+    check_attention(kv, inputs.query(1141 + Hq, 2, Hq), 5)
+
+
+@pytest.mark.parametrize("P", [32, 256])
+def test_int8_attention_page_sizes(P):
+    kv = inputs.paged_kv(1160 + P, [1000, 3 * P + 2], Hkv=8, page_size=P, fill_unused="normal")
+    check_attention(kv, inputs.query(1160 + P, 2, 16), 0)
+
+
+def test_int8_attention_empty_context_and_bad_page_flags():
+    kv = inputs.paged_kv(1170, [40, 40], Hkv=8, page_size=16, fill_unused="normal")
+    kv.context_lens[0] = 0
+    kv.block_table[1, 2] = kv.num_pages + 9
+    k8, v8, ks, vs = int8_cache(kv)
+    of, _ = run_attention(kv, inputs.query(1170, 2, 16), k8, v8, ks, vs)
+    assert pg.device_error_flags() & binding.DEVERR_BAD_PAGE
+    assert np.all(of[0] == 0) and np.isfinite(of).all()
+
+
+def test_int8_prologue_matches_the_oracle():
+    ctx = [40, 17, 64, 1]
+    B = len(ctx)
+    kv = inputs.paged_kv(1180, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    tok = inputs.new_token(1180, B, 16, 8)
+    k8, v8, ks, vs = (np.nan_to_num(a) for a in int8_cache(kv))
+    dev = "cuda"
+    dk8, dv8, dks, dvs = dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs)
+    q_out = torch.empty((B, 16, 128), dtype=torch.bfloat16, device=dev)
+    pg.qk_norm_rope_append_int8(to_device_bf16(tok.q, dev), to_device_bf16(tok.k, dev), to_device_bf16(tok.v, dev),
+                                to_device_bf16(tok.gamma_q, dev), to_device_bf16(tok.gamma_k, dev),
+                                to_device_i32(kv.context_lens, dev), to_device_i32(kv.block_table, dev), dk8, dv8,
+                                dks, dvs, q_out, THETA)
+    torch.cuda.synchronize()
+    q_ref, k8r, v8r, ksr, vsr = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, THETA)
+    assert_bf16_close(bf16_bits(q_out), q_ref, "q_out")
+    gk8, gv8, gks, gvs = dk8.cpu().numpy(), dv8.cpu().numpy(), dks.cpu().numpy(), dvs.cpu().numpy()
+    # V is quantized from the same bf16 row: codes and scales bit for bit
+    assert np.array_equal(gv8, v8r) and np.array_equal(gvs, vsr)
+    # K from the rotated row, whose bf16 rounding may differ by 1 ulp: only the
+    # appended rows change, their codes within 1 step and scales within 2^-7
+    changed = np.any(gk8 != k8, axis=-1) | np.any(k8r != k8, axis=-1) | (gks != ks) | (ksr != ks)
+    assert np.array_equal(gk8[~changed], k8[~changed]) and np.array_equal(gks[~changed], ks[~changed])
+    assert np.abs(gk8.astype(np.int32) - k8r.astype(np.int32)).max() <= 1
+    assert np.all(np.abs(gks - ksr) <= np.abs(ksr) * 2.0 ** -7)
+    assert pg.device_error_flags() == 0
+
+
+def test_int8_prologue_then_attention_chain():
+    ctx = [300, 17, 2049]
+    B = len(ctx)
+    kv = inputs.paged_kv(1190, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    tok = inputs.new_token(1190, B, 16, 8)
+    k8, v8, ks, vs = (np.nan_to_num(a) for a in int8_cache(kv))
+    dev = "cuda"
+    dk8, dv8, dks, dvs = dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs)
+    bt, cl = to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev)
+    q_out = torch.empty((B, 16, 128), dtype=torch.bfloat16, device=dev)
+    pg.qk_norm_rope_append_int8(to_device_bf16(tok.q, dev), to_device_bf16(tok.k, dev), to_device_bf16(tok.v, dev),
+                                to_device_bf16(tok.gamma_q, dev), to_device_bf16(tok.gamma_k, dev), cl, bt, dk8, dv8,
+                                dks, dvs, q_out, THETA)
+    n = pg.decode_attn_int8_workspace_size(B, 16, 8, 128, 16, kv.max_pages, 0)
+    ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+    of = torch.empty((B, 16, 128), dtype=torch.float32, device=dev)
+    ob = torch.empty((B, 16, 128), dtype=torch.bfloat16, device=dev)
+    pg.decode_attn_paged_int8(q_out, dk8, dv8, dks, dvs, bt, cl, SCALE, out_f32=of, out_bf16=ob, workspace=ws)
+    torch.cuda.synchronize()
+    q_ref, k8r, v8r, ksr, vsr = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, THETA)
+    ref = oracle.decode_attention_int8(q_ref, k8r, v8r, ksr, vsr, kv.block_table, kv.context_lens, SCALE)
+    assert np.abs(of.cpu().numpy() - ref).max() <= ATOL_F32
+    own = oracle.decode_attention_int8(bf16_bits(q_out), dk8.cpu().numpy(), dv8.cpu().numpy(), dks.cpu().numpy(),
+                                       dvs.cpu().numpy(), kv.block_table, kv.context_lens, SCALE)
+    assert_bf16_close(bf16_bits(ob), oracle.round_bf16(own), "out_bf16")
+    assert pg.device_error_flags() == 0
+
+
+def test_int8_quality_gate_against_bf16_attention():
+    """INT8 rows (symmetric per row, 8 bits) against the bf16 cache they came
+    from, on N(0,1) keys and values: the attention output stays within 2 %
+    RMS relative error and 0.05 absolute (a bf16 row has 8 significant bits,
+    an INT8 row about 7 relative to its largest element)."""
+    ctx = [4096, 333, 8000]
+    kv = inputs.paged_kv(1200, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    q = inputs.query(1200, len(ctx), 16)
+    k8, v8, ks, vs = int8_cache(kv)
+    of, _ = run_attention(kv, q, k8, v8, ks, vs)
+    ref = oracle.decode_attention(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, SCALE)
+    rms = math.sqrt(float(((of - ref) ** 2).mean() / (ref ** 2).mean()))
+    print(f"INT8 vs bf16 attention: RMS relative {rms:.4f}, max abs {np.abs(of - ref).max():.4f}")
+    assert rms <= 0.02
+    assert np.abs(of - ref).max() <= 0.05

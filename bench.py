@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "ragged_b64", "long_split_kv_t128k", "host_tiled_t64k",
-                             "qwen3_0p6b_t8k_m4"],
+                             "qwen3_0p6b_t8k_m4", "qwen3_0p6b_t8k_int8"],
                     help="the headline step (default) or one of the larger parity workloads, "
                          "measured on their own (one JSON line per variant, not the headline line)")
     ap.add_argument("--layers", type=int, default=None,
@@ -516,6 +516,67 @@ def run_secondary(args):
                   "config": {"B": B, "M": M, "Hq": Hq, "Hkv": Hkv, "T": T, "P": P, "layers": L,
                              "num_partitions": pg.decode_attn_partition_count(B, Hkv, P, max_pages, 0),
                              "l2": "inputs larger than L2: 896 MiB of KV"}})
+        assert pg.device_error_flags() == 0
+        return
+
+    if args.workload == "qwen3_0p6b_t8k_int8":
+        # the Qwen3-shaped 28-layer T = 8192 step over an INT8 cache: per layer
+        # the quantizing prologue and the INT8 attention, one CUDA graph
+        B, Hq, Hkv, T = w["B"], w["Hq"], w["Hkv"], w["T"]
+        L = 28
+        bufs = []
+        for i in range(L):
+            seed = w["seed"] * 1000 + i
+            kv = inputs.paged_kv(seed, [T] * B, Hkv=Hkv, page_size=w["page_size"], spare_pages=0,
+                                 fill_unused="normal")
+            tok = inputs.new_token(seed, B, Hq, Hkv)
+            k8 = torch.from_numpy(inputs.int8_rows(seed, kv.k_cache.shape, 70)).to(dev)
+            v8 = torch.from_numpy(inputs.int8_rows(seed, kv.v_cache.shape, 71)).to(dev)
+            ks = torch.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
+            vs = torch.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
+            bufs.append(dict(k8=k8, v8=v8, ks=ks, vs=vs, bt=to_device_i32(kv.block_table, dev),
+                             ctx=to_device_i32(kv.context_lens, dev), q=to_device_bf16(tok.q, dev),
+                             k=to_device_bf16(tok.k, dev), v=to_device_bf16(tok.v, dev),
+                             gq=to_device_bf16(tok.gamma_q, dev), gk=to_device_bf16(tok.gamma_k, dev),
+                             q_out=torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev),
+                             out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev),
+                             P=kv.page_size, mp=kv.max_pages))
+        n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, bufs[0]["P"], bufs[0]["mp"], 0)
+        ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+
+        def attention_only():
+            for b_ in bufs:
+                pg.decode_attn_paged_int8(b_["q"], b_["k8"], b_["v8"], b_["ks"], b_["vs"], b_["bt"], b_["ctx"], scale,
+                                          out_f32=b_["out"], workspace=ws)
+
+        def step():
+            for b_ in bufs:
+                pg.qk_norm_rope_append_int8(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                            b_["k8"], b_["v8"], b_["ks"], b_["vs"], b_["q_out"], w["theta"])
+                pg.decode_attn_paged_int8(b_["q_out"], b_["k8"], b_["v8"], b_["ks"], b_["vs"], b_["bt"], b_["ctx"],
+                                          scale, out_f32=b_["out"], workspace=ws)
+
+        def capture(fn):
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                fn()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fn()
+            return graph
+
+        int8_bytes = (2 * 128 + 2 * 4) * T * Hkv * L  # codes and scales of K and V
+        bf16_bytes = 4 * T * Hkv * 128 * L
+        for name, fn in (("decode_attn_paged_int8 alone", attention_only),
+                         ("qk_norm_rope_append_int8 + decode_attn_paged_int8", step)):
+            s = timed(capture(fn).replay)
+            emit(f"{name}, {L} layers per graph", int8_bytes, s, peak, "GB/s", peak_kind,
+                 {"us_per_layer_step": s * 1e6 / L, "bf16_equivalent_gbs": bf16_bytes / s / 1e9,
+                  "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "P": bufs[0]["P"], "layers": L,
+                             "bytes_per_row": "128 int8 codes + 1 float scale, K and V",
+                             "l2": "inputs larger than L2: 462 MB of int8 KV"}})
         assert pg.device_error_flags() == 0
         return
 

@@ -268,6 +268,16 @@ __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t bytes, uint32_t sel
     return r;
 }
 
+// As int8x2_to_f16x2 on bytes already biased (xor 0x80808080), so that one
+// bias serves the two halves taken from a register.
+__device__ __forceinline__ uint32_t biased8x2_to_f16x2(uint32_t biased, uint32_t sel)
+{
+    const uint32_t h = __byte_perm(biased, 0x64646464u, sel | 0x4040u);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
 // Two floats -> packed fp16x2 (nearest even); `lo` lands in the low half.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {

@@ -40,7 +40,8 @@ __device__ unsigned g_flags_int8;
 __device__ __forceinline__ void raise_flag8(unsigned f) { atomicOr(&g_flags_int8, f); }
 
 constexpr int kWarps8 = 9;
-constexpr int kStages8 = 3;
+constexpr int kStages8 = 6; // ring of stages per warp: two fold groups, one loading while the other folds
+constexpr int kGroup8 = 3;  // chunks folded together
 constexpr int kTile8 = kChunkTokens * 128;  // 16 rows x 128 int8 codes
 constexpr int kStage8 = 2 * kTile8;         // K tile, V tile
 constexpr int kScaleBytes8 = 2 * kChunkTokens * 4; // K scales, V scales
@@ -65,7 +66,11 @@ struct Int8Params {
 // bf16 kernel: the g <= 8 query heads are the N = 8 columns). Lane (g, t)
 // holds heads 2t, 2t+1 for keys g and g+8 of a chunk; its O^T fragment rows
 // are dims 16mt + 2g and 16mt + 2g + 1 (the permuted M index).
+// With G <= 4 the lo parts of P ride in the spare N columns: column h < 4
+// carries head h's hi part, column 4 + h its lo part (lanes t >= 2), so one
+// PV MMA takes both; the two are added when the record is stored.
 template <int G> struct Int8Warp {
+    static constexpr bool kPackLo = G <= 4;
     uint32_t qb0[8], qb1[8]; // Q^T for k-step ks: dims 16ks+4t, +1 and 16ks+4t+2, +3 of head g (fp16x2)
     float o[8][4];
     float m[2], l[2];
@@ -94,8 +99,8 @@ template <int G> struct Int8Warp {
     // K tile (its V tile follows), scl[c] its 32 scales (16 K, then 16 V),
     // rows[c] its valid rows.
     template <int NC>
-    __device__ __forceinline__ void fold(const uint32_t (&stage)[kStages8], const float *const (&scl)[kStages8],
-                                         const int (&rows)[kStages8], float scale_log2)
+    __device__ __forceinline__ void fold(const uint32_t (&stage)[kGroup8], const float *const (&scl)[kGroup8],
+                                         const int (&rows)[kGroup8], float scale_log2)
     {
         const int lane = threadIdx.x & 31, g = lane >> 2;
         const int mq = lane >> 3, mr = lane & 7;
@@ -119,9 +124,9 @@ template <int G> struct Int8Warp {
                 ldmatrix_x4(r, stage[c] + off);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) { // k-step 2kp + h: matrices 2h (keys 0-7), 2h+1 (keys 8-15)
-                    const uint32_t a[4] = {int8x2_to_f16x2(r[2 * h], 0x100u), int8x2_to_f16x2(r[2 * h + 1], 0x100u),
-                                           int8x2_to_f16x2(r[2 * h], 0x302u),
-                                           int8x2_to_f16x2(r[2 * h + 1], 0x302u)};
+                    const uint32_t r0 = r[2 * h] ^ 0x80808080u, r1 = r[2 * h + 1] ^ 0x80808080u;
+                    const uint32_t a[4] = {biased8x2_to_f16x2(r0, 0x100u), biased8x2_to_f16x2(r1, 0x100u),
+                                           biased8x2_to_f16x2(r0, 0x302u), biased8x2_to_f16x2(r1, 0x302u)};
                     const int ks = 2 * kp + h;
                     mma_f16_16816(h ? sb[c] : sa[c], a, qb0[ks], qb1[ks]);
                 }
@@ -159,12 +164,21 @@ template <int G> struct Int8Warp {
             const float c0 = exp2f(m[0] - mn[0]), c1 = exp2f(m[1] - mn[1]);
             l[0] *= c0;
             l[1] *= c1;
+            float oc0 = c0, oc1 = c1;
+            if constexpr (kPackLo) { // columns 4..7 belong to the heads of lane t - 2
+                const float s0 = __shfl_xor_sync(0xFFFFFFFFu, c0, 2);
+                const float s1 = __shfl_xor_sync(0xFFFFFFFFu, c1, 2);
+                if (lane & 2) {
+                    oc0 = s0;
+                    oc1 = s1;
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-                o[mt][0] *= c0;
-                o[mt][2] *= c0;
-                o[mt][1] *= c1;
-                o[mt][3] *= c1;
+                o[mt][0] *= oc0;
+                o[mt][2] *= oc0;
+                o[mt][1] *= oc1;
+                o[mt][3] *= oc1;
             }
             m[0] = mn[0];
             m[1] = mn[1];
@@ -188,10 +202,17 @@ template <int G> struct Int8Warp {
             const uint32_t hi0 = pack_f16x2(w0, w1), hi1 = pack_f16x2(w2, w3);
             const uint32_t lo0 = pack_f16x2(w0 - f16_lo(hi0), w1 - f16_hi(hi0));
             const uint32_t lo1 = pack_f16x2(w2 - f16_lo(hi1), w3 - f16_hi(hi1));
-            bh0[c] = movmatrix_trans(hi0);
-            bh1[c] = movmatrix_trans(hi1);
-            bl0[c] = movmatrix_trans(lo0);
-            bl1[c] = movmatrix_trans(lo1);
+            if constexpr (kPackLo) {
+                const uint32_t lo0_src = __shfl_xor_sync(0xFFFFFFFFu, lo0, 2);
+                const uint32_t lo1_src = __shfl_xor_sync(0xFFFFFFFFu, lo1, 2);
+                bh0[c] = movmatrix_trans((lane & 2) ? lo0_src : hi0);
+                bh1[c] = movmatrix_trans((lane & 2) ? lo1_src : hi1);
+            } else {
+                bh0[c] = movmatrix_trans(hi0);
+                bh1[c] = movmatrix_trans(hi1);
+                bl0[c] = movmatrix_trans(lo0);
+                bl1[c] = movmatrix_trans(lo1);
+            }
         }
         // O^T += V^T P'^T: ldmatrix.x4.trans covers units u and u+1 of the V
         // tile: matrices (keys 0-7, u), (keys 8-15, u), (0-7, u+1), (8-15, u+1).
@@ -209,11 +230,12 @@ template <int G> struct Int8Warp {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int mt = 2 * up + h;
-                    const uint32_t a[4] = {int8x2_to_f16x2(r[2 * h], 0x200u), int8x2_to_f16x2(r[2 * h], 0x301u),
-                                           int8x2_to_f16x2(r[2 * h + 1], 0x200u),
-                                           int8x2_to_f16x2(r[2 * h + 1], 0x301u)};
+                    const uint32_t r0 = r[2 * h] ^ 0x80808080u, r1 = r[2 * h + 1] ^ 0x80808080u;
+                    const uint32_t a[4] = {biased8x2_to_f16x2(r0, 0x200u), biased8x2_to_f16x2(r0, 0x301u),
+                                           biased8x2_to_f16x2(r1, 0x200u), biased8x2_to_f16x2(r1, 0x301u)};
                     mma_f16_16816(o[mt], a, bh0[c], bh1[c]);
-                    mma_f16_16816(o[mt], a, bl0[c], bl1[c]);
+                    if constexpr (!kPackLo)
+                        mma_f16_16816(o[mt], a, bl0[c], bl1[c]);
                 }
             }
         }
@@ -223,6 +245,13 @@ template <int G> struct Int8Warp {
     __device__ __forceinline__ void store_record(float *rec)
     {
         const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+        if constexpr (kPackLo) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[mt][e] += __shfl_xor_sync(0xFFFFFFFFu, o[mt][e], 2);
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             l[c] += __shfl_xor_sync(0xFFFFFFFFu, l[c], 4);
@@ -364,12 +393,12 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     bool ok = true;
     int k0 = 0;
     for (int nc; k0 < my_chunks; k0 += nc) {
-        nc = min(kStages8, my_chunks - k0);
-        uint32_t stage_addr[kStages8];
-        const float *scl[kStages8];
-        int rows[kStages8];
+        nc = min(kGroup8, my_chunks - k0);
+        uint32_t stage_addr[kGroup8];
+        const float *scl[kGroup8];
+        int rows[kGroup8];
 #pragma unroll
-        for (int c = 0; c < kStages8; ++c) {
+        for (int c = 0; c < kGroup8; ++c) {
             const int k = k0 + c;
             stage_addr[c] = smem_addr(stages + (k % kStages8) * kStage8);
             scl[c] = scales + (k % kStages8) * 2 * kChunkTokens;
@@ -391,7 +420,7 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
             st.template fold<1>(stage_addr, scl, rows, p.scale_log2);
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < kStages8; ++c) {
+        for (int c = 0; c < kGroup8; ++c) {
             const int k = k0 + c + kStages8;
             if (c < nc && k < my_chunks) {
                 const int phys = phys_of(k);

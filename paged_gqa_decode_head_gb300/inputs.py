@@ -158,6 +158,11 @@ def query(seed: int, B: int, Hq: int, D: int = 128, stream: int = 20) -> np.ndar
     return normal_bf16(generator(seed, stream), (B, Hq, D))
 
 
+def int8_rows(seed: int, shape, stream: int) -> np.ndarray:
+    """Uniform int8 codes in [-127, 127] (an INT8 cache's rows for timing)."""
+    return generator(seed, stream).integers(-127, 128, size=shape, dtype=np.int8)
+
+
 def ragged_lengths(seed: int, B: int, lo: int, hi: int, stream: int = 30) -> np.ndarray:
     """Per-sequence context lengths ~ U[lo, hi] (integers, both ends included)."""
     return generator(seed, stream).integers(lo, hi + 1, size=B).astype(np.int32)
@@ -198,6 +203,7 @@ WORKLOADS = {
     "long_split_kv_t128k": dict(seed=1003, B=1, Hq=32, Hkv=8, D=128, T=131072, page_size=16,
                                 partition=512, outlier_fraction=0.01, outlier_factor=8.0),
     "host_tiled_t64k": dict(seed=1004, B=1, Hq=16, Hkv=8, D=128, T=65536, tile=512),
+    "qwen3_0p6b_t8k_int8": dict(seed=1006, layers=28, B=1, Hq=16, Hkv=8, D=128, T=8192, page_size=16, theta=1e6),
     "qwen3_0p6b_t8k_m4": dict(seed=1005, layers=28, B=1, M=4, Hq=16, Hkv=8, D=128, T=8192, page_size=16,
                               theta=1e6),
 }

@@ -462,6 +462,22 @@ def run_secondary(args):
                  kv_bytes, s, peak, "GB/s", peak_kind,
                  {"config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "kv_bytes": kv_bytes,
                              "l2": "inputs larger than L2"}})
+        # the same workload over an INT8 cache (timing only: uniform codes,
+        # scales 1/127; parity is the test suite's)
+        del kc, vc
+        k8 = torch.from_numpy(inputs.int8_rows(w["seed"], kv.k_cache.shape, 72)).to(dev)
+        v8 = torch.from_numpy(inputs.int8_rows(w["seed"], kv.v_cache.shape, 73)).to(dev)
+        ks = torch.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
+        vs = torch.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
+        int8_bytes = kv_bytes // 512 * (2 * 128 + 2 * 4)
+        n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, 0)
+        ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+        s = timed(lambda: pg.decode_attn_paged_int8(qd, k8, v8, ks, vs, bt, ctx, scale, out_f32=out, workspace=ws))
+        emit(f"decode_attn_paged_int8 NP={pg.decode_attn_partition_count(B, Hkv, kv.page_size, kv.max_pages, 0)} "
+             "(automatic)", int8_bytes, s, peak, "GB/s", peak_kind,
+             {"bf16_equivalent_gbs": kv_bytes / s / 1e9,
+              "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "int8_bytes": int8_bytes,
+                         "l2": "inputs larger than L2"}})
         assert pg.device_error_flags() == 0
         return
 

@@ -572,6 +572,12 @@ def run_secondary(args):
                 pg.decode_attn_paged_int8(b_["q_out"], b_["k8"], b_["v8"], b_["ks"], b_["vs"], b_["bt"], b_["ctx"],
                                           scale, out_f32=b_["out"], workspace=ws)
 
+        def fused():
+            for b_ in bufs:
+                pg.decode_step_paged_int8(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                          b_["k8"], b_["v8"], b_["ks"], b_["vs"], scale, w["theta"],
+                                          q_out=b_["q_out"], out_f32=b_["out"], workspace=ws)
+
         def capture(fn):
             side = torch.cuda.Stream(dev)
             side.wait_stream(torch.cuda.current_stream(dev))
@@ -585,7 +591,8 @@ def run_secondary(args):
 
         int8_bytes = (2 * 128 + 2 * 4) * T * Hkv * L  # codes and scales of K and V
         bf16_bytes = 4 * T * Hkv * 128 * L
-        for name, fn in (("decode_attn_paged_int8 alone", attention_only),
+        for name, fn in (("decode_step_paged_int8 (one launch per layer)", fused),
+                         ("decode_attn_paged_int8 alone", attention_only),
                          ("qk_norm_rope_append_int8 + decode_attn_paged_int8", step)):
             s = timed(capture(fn).replay)
             emit(f"{name}, {L} layers per graph", int8_bytes, s, peak, "GB/s", peak_kind,

@@ -276,7 +276,10 @@ int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const 
  *   attention with every key and value row dequantized. The query must lie
  *   in the fp16 range (|q| < 65504; the fold runs fp16 tensor-core MMAs).
  *   Reading and PDL rules as decode_attn_paged; workspace of
- *   decode_attn_int8_workspace_size bytes (no initial value needed).
+ *   decode_attn_int8_workspace_size bytes with decode_attn_paged's rules
+ *   (zero-filled before the first call with given arguments, left ready by
+ *   every completed call, not shared by calls that may overlap); with up to
+ *   64 partitions the last CTA of each (sequence, KV head) merges them.
  */
 int qk_norm_rope_append_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
                              const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
@@ -291,6 +294,30 @@ int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int
                            const int32_t *context_lens, int B, int Hq, int Hkv, int D, int page_size,
                            int max_pages, int num_pages, float scale, int num_partitions, float *out_f32,
                            pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * decode_step_paged_int8 -- qk_norm_rope_append_int8 followed by
+ * decode_attn_paged_int8 in one launch, with the same results as calling the
+ * two in order (as decode_step_paged is for the bf16 cache). Each attention
+ * CTA normalises and rotates the query heads it serves; the CTA whose
+ * partition holds position T_b - 1 quantizes the new K and V rows and writes
+ * their codes and scales to the cache.
+ *
+ *   q, k, v, gamma_q, gamma_k, context_lens (T_b >= 1), block_table,
+ *   k_cache8, v_cache8, k_scale, v_scale, rope_theta, eps
+ *                                   as for qk_norm_rope_append_int8
+ *   q_out    [B][Hq][D] bf16, nullable: the rotated query, if wanted
+ *   scale, num_partitions, out_f32, out_bf16, workspace, ws_bytes
+ *                                   as for decode_attn_paged_int8
+ * Sequences with T_b < 1 raise PGQA_DEVERR_BAD_CONTEXT and produce zeros.
+ */
+int decode_step_paged_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                           const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k, const int32_t *context_lens,
+                           const int32_t *block_table, int8_t *k_cache8, int8_t *v_cache8, float *k_scale,
+                           float *v_scale, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages, float rope_theta, float eps, float scale,
+                           int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream);
 
 /*
  * attn_partition_merge -- exact merge of NP partition states (s9.1).

@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     decode_attn_paged_multi,
     decode_attn_paged_static,
     decode_step_paged,
+    decode_step_paged_int8,
     decode_step_paged_multi,
     decode_attn_partition_count,
     decode_attn_workspace_size,

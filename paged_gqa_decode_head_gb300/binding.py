@@ -36,6 +36,7 @@ EXPORTED = (
     "qk_norm_rope_append_int8",
     "decode_attn_int8_workspace_size",
     "decode_attn_paged_int8",
+    "decode_step_paged_int8",
     "attn_partition_merge",
     "attn_tile_init",
     "attn_tile_update",
@@ -101,6 +102,8 @@ def load_library():
         lib.decode_attn_int8_workspace_size.restype = S
         lib.decode_attn_paged_int8.argtypes = [P] * 7 + [I] * 7 + [F, I, P, P, P, S, P]
         lib.decode_attn_paged_int8.restype = I
+        lib.decode_step_paged_int8.argtypes = [P] * 12 + [I] * 7 + [F, F, F, I, P, P, P, S, P]
+        lib.decode_step_paged_int8.restype = I
         lib.qk_norm_rope_append.restype = I
         lib.decode_attn_partition_count.argtypes = [I] * 5
         lib.decode_attn_partition_count.restype = I
@@ -325,6 +328,27 @@ def decode_attn_paged_int8(q, k_cache8, v_cache8, k_scale, v_scale, block_table,
         _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True), ws_ptr, ws_bytes,
         _stream(stream))
     _check("decode_attn_paged_int8", st)
+
+
+def decode_step_paged_int8(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache8, v_cache8, k_scale,
+                           v_scale, scale: float, rope_theta: float, eps: float = 1e-6, q_out=None, out_f32=None,
+                           out_bf16=None, workspace=None, num_partitions: int = 0, stream=None) -> None:
+    """Fused qk_norm_rope_append_int8 + decode_attn_paged_int8 for one layer (one launch)."""
+    lib = load_library()
+    bf, i32, i8, f32 = torch.bfloat16, torch.int32, torch.int8, torch.float32
+    B, Hq, D = q.shape
+    num_pages, Hkv, P, _ = k_cache8.shape
+    ws_ptr = _dev(workspace, torch.uint8, "workspace", nullable=True)
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    st = lib.decode_step_paged_int8(
+        _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(gamma_q, bf, "gamma_q"),
+        _dev(gamma_k, bf, "gamma_k"), _dev(context_lens, i32, "context_lens"), _dev(block_table, i32, "block_table"),
+        _dev(k_cache8, i8, "k_cache8"), _dev(v_cache8, i8, "v_cache8"), _dev(k_scale, f32, "k_scale"),
+        _dev(v_scale, f32, "v_scale"), _dev(q_out, bf, "q_out", nullable=True), B, Hq, Hkv, D, P,
+        block_table.shape[1], num_pages, float(rope_theta), float(eps), float(scale), int(num_partitions),
+        _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check("decode_step_paged_int8", st)
 
 
 def decode_step_paged(q, k, v, gamma_q, gamma_k, context_lens, block_table, k_cache, v_cache, scale: float,

@@ -715,16 +715,21 @@ size_t decode_attn_int8_workspace_size(int B, int Hq, int Hkv, int D, int page_s
         return 0;
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    return pgqa::decode_int8_workspace_bytes(B, Hq, np);
+    return pgqa::decode_int8_workspace_bytes(B, Hkv, Hq, np);
 }
 
-int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int8_t *v_cache8,
-                           const float *k_scale, const float *v_scale, const int32_t *block_table,
-                           const int32_t *context_lens, int B, int Hq, int Hkv, int D, int page_size,
-                           int max_pages, int num_pages, float scale, int num_partitions, float *out_f32,
-                           pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream)
+// Validation, partition choice and launch shared by decode_attn_paged_int8
+// (fused = false: q is the rotated query) and decode_step_paged_int8 (fused:
+// q, k, v are the new token's raw heads and the kernel appends to the cache).
+static int int8_attn_impl(const char *fn, bool fused, const pgqa_bf16 *q, const pgqa_bf16 *k,
+                          const pgqa_bf16 *v, const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,
+                          const int8_t *k_cache8, const int8_t *v_cache8, const float *k_scale,
+                          const float *v_scale, const int32_t *block_table, const int32_t *context_lens,
+                          pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                          int num_pages, float rope_theta, float eps, float scale, int num_partitions,
+                          float *out_f32, pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes,
+                          cudaStream_t stream)
 {
-    const char *fn = "decode_attn_paged_int8";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
     if (int st = check_pages(fn, page_size, max_pages, num_pages))
@@ -733,21 +738,26 @@ int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int
         return fail(PGQA_ERR_INVALID_ARG, "%s: num_partitions must be >= 0", fn);
     if (!std::isfinite(scale))
         return fail(PGQA_ERR_INVALID_ARG, "%s: scale is not finite", fn);
+    if (fused && (!(rope_theta > 0.f) || !std::isfinite(rope_theta) || !(eps >= 0.f) || !std::isfinite(eps)))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: rope_theta must be > 0 and eps >= 0", fn);
     if (static_cast<long long>(num_pages) * Hkv * page_size > 0x7FFFFFFFLL)
         return fail(PGQA_ERR_UNSUPPORTED, "%s: num_pages * Hkv * page_size exceeds 2^31 - 1 rows", fn);
     if (B == 0)
         return ok();
-    if (!q || !k_cache8 || !v_cache8 || !k_scale || !v_scale || !block_table || !context_lens)
+    if (!q || !k_cache8 || !v_cache8 || !k_scale || !v_scale || !block_table || !context_lens ||
+        (fused && (!k || !v || !gamma_q || !gamma_k)))
         return fail(PGQA_ERR_INVALID_ARG, "%s: a required pointer is NULL", fn);
     if (!out_f32 && !out_bf16)
         return fail(PGQA_ERR_INVALID_ARG, "%s: out_f32 and out_bf16 are both NULL", fn);
     if (!aligned16(q) || !aligned16(k_cache8) || !aligned16(v_cache8) || !aligned16(k_scale) ||
         !aligned16(v_scale) || (out_f32 && !aligned16(out_f32)) || (out_bf16 && !aligned16(out_bf16)) ||
-        !aligned4(block_table) || !aligned4(context_lens) || (workspace && !aligned16(workspace)))
+        !aligned4(block_table) || !aligned4(context_lens) || (workspace && !aligned16(workspace)) ||
+        (fused && (!aligned16(k) || !aligned16(v) || !aligned16(gamma_q) || !aligned16(gamma_k) ||
+                   (q_out && !aligned16(q_out)))))
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte and index arrays 4-byte alignment", fn);
     const int np = pgqa::choose_partitions(B, Hkv, page_size, max_pages, num_partitions,
                                            sm_count_current_device());
-    const size_t need = pgqa::decode_int8_workspace_bytes(B, Hq, np);
+    const size_t need = pgqa::decode_int8_workspace_bytes(B, Hkv, Hq, np);
     if (need > 0 && (!workspace || ws_bytes < need))
         return fail(PGQA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for %d partitions, got %zu", fn, need,
                     np, workspace ? ws_bytes : static_cast<size_t>(0));
@@ -771,10 +781,47 @@ int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int
     a.out_f32 = out_f32;
     a.out_bf16 = out_bf16;
     a.ws = static_cast<float *>(workspace);
+    if (fused) {
+        a.fused = true;
+        a.q_raw = q;
+        a.k_new = k;
+        a.v_new = v;
+        a.gamma_q = gamma_q;
+        a.gamma_k = gamma_k;
+        a.q_out = q_out;
+        a.rope_theta = static_cast<double>(rope_theta);
+        a.eps = eps;
+    }
     cudaError_t err = pgqa::launch_decode_int8(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
     return ok();
+}
+
+int decode_attn_paged_int8(const pgqa_bf16 *q, const int8_t *k_cache8, const int8_t *v_cache8,
+                           const float *k_scale, const float *v_scale, const int32_t *block_table,
+                           const int32_t *context_lens, int B, int Hq, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages, float scale, int num_partitions, float *out_f32,
+                           pgqa_bf16 *out_bf16, void *workspace, size_t ws_bytes, cudaStream_t stream)
+{
+    return int8_attn_impl("decode_attn_paged_int8", false, q, nullptr, nullptr, nullptr, nullptr, k_cache8,
+                          v_cache8, k_scale, v_scale, block_table, context_lens, nullptr, B, Hq, Hkv, D,
+                          page_size, max_pages, num_pages, 1.0f, 0.0f, scale, num_partitions, out_f32, out_bf16,
+                          workspace, ws_bytes, stream);
+}
+
+int decode_step_paged_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
+                           const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k, const int32_t *context_lens,
+                           const int32_t *block_table, int8_t *k_cache8, int8_t *v_cache8, float *k_scale,
+                           float *v_scale, pgqa_bf16 *q_out, int B, int Hq, int Hkv, int D, int page_size,
+                           int max_pages, int num_pages, float rope_theta, float eps, float scale,
+                           int num_partitions, float *out_f32, pgqa_bf16 *out_bf16, void *workspace,
+                           size_t ws_bytes, cudaStream_t stream)
+{
+    return int8_attn_impl("decode_step_paged_int8", true, q, k, v, gamma_q, gamma_k, k_cache8, v_cache8, k_scale,
+                          v_scale, block_table, context_lens, q_out, B, Hq, Hkv, D, page_size, max_pages,
+                          num_pages, rope_theta, eps, scale, num_partitions, out_f32, out_bf16, workspace,
+                          ws_bytes, stream);
 }
 
 } // extern "C"

@@ -44,6 +44,7 @@
 #include "attn_core.cuh"
 #include "head_norm_rope.cuh"
 #include "launch.h"
+#include "partition_merge.cuh"
 
 namespace pgqa {
 namespace {
@@ -72,11 +73,12 @@ constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
 constexpr int kTicketOffset = (kRowsOffset + kWarps * kStages * 4 + 7) & ~7;
 constexpr int kMergeBarOffset = kTicketOffset + 8;
 constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
-constexpr int kSplitSmem = 1024 /* alignment slack */ + kQBufOffset + kMaxGroup * kHeadDim * 2;
+constexpr int kPatchOffset = kQBufOffset + kMaxGroup * kHeadDim * 2; // fused step: new K, V rows (bf16)
+constexpr int kSplitSmem = 1024 /* alignment slack */ + kPatchOffset + 4 * kHeadDim;
 // The in-kernel merge copies the G x n partition accumulators of its group
 // into the stage area, followed by its scratch (weights, sums, a float4 per
 // thread); launch_decode falls back to merge_kernel when they do not fit.
-constexpr int kMergeScratchBytes = kMaxGroup * kFusedMergeMax * 4 + 64 + kWarps * 32 * 16;
+constexpr int kMergeScratchBytes = merge_scratch_bytes<kWarps * 32, kFusedMergeMax>(kMaxGroup);
 
 struct SplitParams {
     const uint16_t *q;
@@ -302,104 +304,16 @@ template <int NCOL> struct MmaWarp {
 };
 
 // The last CTA of a (sequence, KV head) to finish merges the n (2..64)
-// partition states of its G query heads from the workspace (base-2 m) and
-// writes the outputs, in one round trip to memory: thread 0 copies the G x n
-// accumulators into shared memory (one bulk copy per head) while one warp per
-// head loads m and l and forms the weights e^(m_p - M) and L with shuffles;
-// then every thread folds its share of the accumulators from shared memory.
+// partition states of its columns (partition_merge.cuh).
 template <int NCOL, bool kMulti>
-__device__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n, unsigned char *smem,
-                                  uint64_t *bar)
+__device__ __forceinline__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n,
+                                                  unsigned char *smem, uint64_t *bar)
 {
-    constexpr int kThreads = kWarps * 32;
-    float *acc = reinterpret_cast<float *>(smem);            // [NCOL][n][128]
-    float *w = acc + static_cast<size_t>(NCOL) * n * kHeadDim; // [NCOL][kFusedMergeMax] weights
-    float *Ls = w + NCOL * kFusedMergeMax;                     // [NCOL], padded to 16 floats
-    float4 *red = reinterpret_cast<float4 *>(Ls + 16);      // [kThreads] partial sums
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        // the stage area was last used through the generic proxy, and the
-        // other CTAs' partition states were acquired through it
-        fence_proxy_async_smem();
-        fence_proxy_async_global();
-        const uint32_t row_bytes = static_cast<uint32_t>(n) * kHeadDim * 4;
-        mbar_arrive_expect_tx(bar, NCOL * row_bytes);
-#pragma unroll
-        for (int h = 0; h < NCOL; ++h)
-            bulk_copy_g2s_nohint(acc + static_cast<size_t>(h) * n * kHeadDim,
-                                 p.ws_acc + column_row<kMulti>(p, b, kvh, h) * p.NP * kHeadDim, row_bytes, bar);
-    }
-    for (int h = warp; h < NCOL; h += kWarps) {
-        const float *mh = p.ws_m + column_row<kMulti>(p, b, kvh, h) * p.NP;
-        const float *lh = p.ws_l + column_row<kMulti>(p, b, kvh, h) * p.NP;
-        const float m0 = lane < n ? __ldcg(mh + lane) : kEmptyMax;
-        const float m1 = lane + 32 < n ? __ldcg(mh + lane + 32) : kEmptyMax;
-        const float l0 = lane < n ? __ldcg(lh + lane) : 0.f;
-        const float l1 = lane + 32 < n ? __ldcg(lh + lane + 32) : 0.f;
-        float M = fmaxf(m0, m1);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-        const float w0 = exp2f(m0 - M), w1 = exp2f(m1 - M);
-        float L = l0 * w0 + l1 * w1;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            L += __shfl_xor_sync(0xFFFFFFFFu, L, off);
-        w[h * kFusedMergeMax + lane] = w0;
-        w[h * kFusedMergeMax + lane + 32] = w1;
-        if (lane == 0)
-            Ls[h] = L;
-    }
-    __syncthreads();
-    if (!mbar_wait_bounded(bar, 0)) {
-        // The copy never completed: flag it, give it one more bounded wait
-        // (it writes this CTA's shared memory) and leave the outputs alone.
-        if (threadIdx.x == 0)
-            raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
-        (void)mbar_wait_bounded(bar, 0);
-        return;
-    }
-    constexpr int kItems = NCOL * 32; // (column, 4 dims)
-    constexpr int kSlices = kThreads >= kItems ? kThreads / kItems : 1;
-    constexpr int kLanesPerSlice = kThreads / kSlices;
-    for (int base = 0; base < kItems; base += kLanesPerSlice) {
-        const int item = base + (threadIdx.x % kLanesPerSlice);
-        const int slice = threadIdx.x / kLanesPerSlice;
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (item < kItems && slice < kSlices) {
-            const int h = item / 32, d4 = item % 32;
-            const float4 *src = reinterpret_cast<const float4 *>(acc + static_cast<size_t>(h) * n * kHeadDim) + d4;
-            for (int part = slice; part < n; part += kSlices) {
-                const float4 v = src[static_cast<size_t>(part) * (kHeadDim / 4)];
-                const float wt = w[h * kFusedMergeMax + part];
-                sum.x = fmaf(v.x, wt, sum.x);
-                sum.y = fmaf(v.y, wt, sum.y);
-                sum.z = fmaf(v.z, wt, sum.z);
-                sum.w = fmaf(v.w, wt, sum.w);
-            }
-        }
-        red[threadIdx.x] = sum;
-        __syncthreads();
-        if (slice == 0 && item < kItems) {
-            for (int sl = 1; sl < kSlices; ++sl) {
-                const float4 v = red[threadIdx.x + sl * kLanesPerSlice];
-                sum.x += v.x, sum.y += v.y, sum.z += v.z, sum.w += v.w;
-            }
-            const int h = item / 32, d4 = item % 32;
-            const float L = Ls[h];
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const float r[4] = {sum.x * inv, sum.y * inv, sum.z * inv, sum.w * inv};
-            const size_t off = column_row<kMulti>(p, b, kvh, h) * kHeadDim + 4 * d4;
-            if (p.out_f32)
-                *reinterpret_cast<float4 *>(p.out_f32 + off) = make_float4(r[0], r[1], r[2], r[3]);
-            if (p.out_bf16)
-                *reinterpret_cast<uint2 *>(p.out_bf16 + off) =
-                    make_uint2(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]));
-        }
-        __syncthreads();
-    }
+    const auto row_of = [&](int c) { return column_row<kMulti>(p, b, kvh, c); };
+    if (!merge_partitions_in_cta<NCOL, kWarps * 32, kFusedMergeMax>(p.ws_m, p.ws_l, p.ws_acc, p.NP, n, row_of,
+                                                                     p.out_f32, p.out_bf16, smem, bar) &&
+        threadIdx.x == 0)
+        raise_flag(PGQA_DEVERR_WAIT_TIMEOUT); // the merge's copy never landed: outputs left alone
 }
 
 // kFused = true: the whole decode step of one layer (qk_norm_rope_append
@@ -523,9 +437,10 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 
     // fused step: what the prologue needs that no earlier kernel writes
     // (gains, rotation, the append slot) is prepared before the wait.
-    // Single token (kMulti = false): warps < G rotate the query heads; the
-    // warp owning the chunk of position T-1 computes the new K row, appends K
-    // and V and patches the row into its staged chunk. M tokens (kMulti):
+    // Single token (kMulti = false): warps < G rotate the query heads; once
+    // every warp has its query, the warp owning the chunk of position T-1
+    // computes the new K row, appends K and V and keeps the row in shared
+    // memory to patch it into its staged chunk. M tokens (kMulti):
     // warp w < NCOL rotates column w (token w / G, head w % G) and warp w < M
     // appends token w at T - M + w; chunks holding new positions are
     // requested only once every append is done.
@@ -597,7 +512,6 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncwarp();
 
     // fused step: normalise and rotate q and the new K rows, append K and V.
-    uint16_t new_k[4] = {0, 0, 0, 0};
     if constexpr (kFused) {
         uint16_t *q_buf = reinterpret_cast<uint16_t *>(smem + kQBufOffset);
         if (has_q) {
@@ -610,18 +524,15 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                     p.q_out[qrow + lane + 32 * i] = bits;
             }
         }
-        if (appends) {
+        if (kMulti && appends) {
+            // M tokens: appended before the barrier, their chunks requested after it
             norm_rope_apply(xk, gain_k, p.eps, rope_k);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                new_k[i] = f32_to_bf16_bits(xk[i]);
-            const int apos = kMulti ? tok_pos : pos;
             if (new_phys >= 0 && new_phys < p.num_pages) {
                 const size_t slot =
-                    ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + apos % p.P) * kHeadDim;
+                    ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + tok_pos % p.P) * kHeadDim;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    p.k_cache[slot + lane + 32 * i] = new_k[i];
+                    p.k_cache[slot + lane + 32 * i] = f32_to_bf16_bits(xk[i]);
                     p.v_cache[slot + lane + 32 * i] = new_v[i];
                 }
             } else if (lane == 0) {
@@ -641,6 +552,28 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
             __syncwarp();
         }
         st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
+        if (!kMulti && appends) {
+            // single token: off the other warps' path; the row waits in
+            // shared memory for the patch of its staged chunk
+            uint16_t *patch = reinterpret_cast<uint16_t *>(smem + kPatchOffset);
+            norm_rope_apply(xk, gain_k, p.eps, rope_k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                patch[lane + 32 * i] = f32_to_bf16_bits(xk[i]);
+                patch[kHeadDim + lane + 32 * i] = new_v[i];
+            }
+            if (new_phys >= 0 && new_phys < p.num_pages) {
+                const size_t slot = ((static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + pos % p.P) * kHeadDim;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    p.k_cache[slot + lane + 32 * i] = patch[lane + 32 * i];
+                    p.v_cache[slot + lane + 32 * i] = new_v[i];
+                }
+            } else if (lane == 0) {
+                raise_flag(PGQA_DEVERR_BAD_PAGE);
+            }
+            __syncwarp();
+        }
     }
 
     // Causal limit (exclusive position) of this lane's columns 2t and 2t+1:
@@ -674,15 +607,19 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
                 rows[c] = stage_rows[k % kStages];
                 if (kFused && k == new_chunk && rows[c] > 0) {
                     // the staged copy predates the append: put the new row in
+                    // (word w < 128 of the patch: K dims 2w, 2w+1 for w < 64,
+                    // then V dims 2(w-64), 2(w-64)+1)
                     const int r = (T - 1) % kChunkTokens;
                     unsigned char *stage = stages + (k % kStages) * kStageBytes;
+                    const uint32_t *patch = reinterpret_cast<const uint32_t *>(smem + kPatchOffset);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int d = lane + 32 * i;
+                        const int w = lane + 32 * i;
+                        const int d = 2 * (w & 63);
                         const int x = d & 63, u = x >> 3;
-                        const int off = (d >> 6) * kBoxBytes + r * 128 + ((u ^ (r & 7)) << 4) + (x & 7) * 2;
-                        *reinterpret_cast<uint16_t *>(stage + off) = new_k[i];
-                        *reinterpret_cast<uint16_t *>(stage + 2 * kBoxBytes + off) = new_v[i];
+                        const int off = (w >> 6) * 2 * kBoxBytes + (d >> 6) * kBoxBytes + r * 128 +
+                                        ((u ^ (r & 7)) << 4) + (x & 7) * 2;
+                        *reinterpret_cast<uint32_t *>(stage + off) = patch[w];
                     }
                     __syncwarp();
                 }

@@ -20,9 +20,16 @@
 // row, so the MMA's k index (S^T = K Q^T) and M index (O^T = V^T P^T) are
 // taken in a fixed permutation of the 16 dims of a step -- the query is loaded
 // in the same permutation and the output rows are stored back in dim order.
+// With kFused the kernel is the whole decode step (decode_step_paged_int8):
+// each CTA normalises and rotates its query heads, the warp whose chunk holds
+// position T-1 quantizes the new K and V rows, appends them and patches them
+// into its staged chunk (as the bf16 fused step does), so every history chunk
+// may be requested before griddepcontrol.wait.
 // Per-key K scales multiply the scores; per-key V scales are folded into P,
 // which is split into fp16 hi + lo parts. Partition states go to the
-// workspace and merge_kernel merges them.
+// workspace; the last CTA of a (sequence, KV head) to finish merges them
+// (partition_merge.cuh), or merge_kernel does when they do not fit its
+// shared memory.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
@@ -30,7 +37,10 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "head_norm_rope.cuh"
 #include "launch.h"
+#include "partition_merge.cuh"
+#include "quantize_int8.cuh"
 
 namespace pgqa {
 namespace {
@@ -39,17 +49,41 @@ __device__ unsigned g_flags_int8;
 
 __device__ __forceinline__ void raise_flag8(unsigned f) { atomicOr(&g_flags_int8, f); }
 
-constexpr int kWarps8 = 9;
-constexpr int kStages8 = 6; // ring of stages per warp: two fold groups, one loading while the other folds
-constexpr int kGroup8 = 3;  // chunks folded together
-constexpr int kTile8 = kChunkTokens * 128;  // 16 rows x 128 int8 codes
-constexpr int kStage8 = 2 * kTile8;         // K tile, V tile
+constexpr int kTile8 = kChunkTokens * 128;         // 16 rows x 128 int8 codes
+constexpr int kStage8 = 2 * kTile8;                // K tile, V tile
 constexpr int kScaleBytes8 = 2 * kChunkTokens * 4; // K scales, V scales
-constexpr int kStageArea8 = kWarps8 * kStages8 * kStage8;
-constexpr int kScaleOffset8 = kStageArea8;
-constexpr int kBarOffset8 = kScaleOffset8 + kWarps8 * kStages8 * kScaleBytes8;
-constexpr int kRowsOffset8 = kBarOffset8 + kWarps8 * kStages8 * 8;
-constexpr int kSmem8 = 1024 /* alignment slack */ + kRowsOffset8 + kWarps8 * kStages8 * 4;
+constexpr int kFusedMergeMax8 = 64;                // partitions the last CTA merges itself
+// Partitions of at least this many chunks use the 12-warp shape.
+constexpr int kDeepChunks8 = 64;
+
+// CTA shapes: kW warps, each owning every kW-th chunk of its partition in a
+// ring of kStages stages folded kGroup at a time (two groups: one loads while
+// the other folds). 9 warps x 6 stages suit short partitions (the T = 8192
+// layer chain: 3 chunks per warp, all in flight at once); 12 warps x 4 stages
+// spread evenly over the SM's four sub-partitions (9 warps leave one of them
+// with three), which long partitions, bound by the fold, need.
+template <int kW> struct Shape8 {
+    static constexpr int kWarps = kW;
+    static constexpr int kStages = kW == 12 ? 4 : 6;
+    static constexpr int kGroup = kStages / 2; // chunks folded together
+    static constexpr int kStageArea = kWarps * kStages * kStage8;
+    static constexpr int kScaleOffset = kStageArea;
+    static constexpr int kBarOffset = kScaleOffset + kWarps * kStages * kScaleBytes8;
+    static constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
+    static constexpr int kTicketOffset = (kRowsOffset + kWarps * kStages * 4 + 7) & ~7;
+    static constexpr int kMergeBarOffset = kTicketOffset + 8;
+    // fused step: the rotated query [G][128] bf16, then the appended row as
+    // it goes into its staged chunk (K codes, V codes [128] each, the K and V
+    // scales)
+    static constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
+    static constexpr int kPatchOffset = kQBufOffset + kMaxGroup * kHeadDim * 2;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kPatchOffset + 2 * kHeadDim + 16;
+    static constexpr int kMergeScratch = merge_scratch_bytes<kWarps * 32, kFusedMergeMax8>(kMaxGroup);
+    // chunks per warp requested before griddepcontrol.wait
+    template <bool kFused> static constexpr int kPrewait = kFused ? 2 : kStages;
+    static_assert(kSmem <= 232448, "exceeds the 227 KiB of shared memory a CTA may hold");
+    static_assert(kGroup >= 1 && kGroup <= 3, "fold groups of 1 to 3 chunks");
+};
 
 struct Int8Params {
     const uint16_t *q;
@@ -58,8 +92,18 @@ struct Int8Params {
     float *out_f32;
     uint16_t *out_bf16;
     float *ws_m, *ws_l, *ws_acc;
+    unsigned *tickets; // [B*Hkv] partition tickets (in-kernel merge)
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
+    int fused_merge;
     float scale_log2;
+    // fused decode step only: the new token's raw heads, the prologue's
+    // parameters and the cache to append to
+    const uint16_t *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
+    int8_t *k_cache8, *v_cache8;
+    float *k_scale_out, *v_scale_out;
+    uint16_t *q_out;
+    float eps;
+    RopeFreqs freqs;
 };
 
 // Per-warp online-softmax state on fp16 MMA fragments (transposed as in the
@@ -98,9 +142,9 @@ template <int G> struct Int8Warp {
     // Fold NC resident chunks: stage[c] is the shared address of chunk c's
     // K tile (its V tile follows), scl[c] its 32 scales (16 K, then 16 V),
     // rows[c] its valid rows.
-    template <int NC>
-    __device__ __forceinline__ void fold(const uint32_t (&stage)[kGroup8], const float *const (&scl)[kGroup8],
-                                         const int (&rows)[kGroup8], float scale_log2)
+    template <int NC, int NG>
+    __device__ __forceinline__ void fold(const uint32_t (&stage)[NG], const float *const (&scl)[NG],
+                                         const int (&rows)[NG], float scale_log2)
     {
         const int lane = threadIdx.x & 31, g = lane >> 2;
         const int mq = lane >> 3, mr = lane & 7;
@@ -285,11 +329,12 @@ template <int G> struct Int8Warp {
     }
 };
 
-template <int G>
-__global__ void __launch_bounds__(kWarps8 * 32, 1)
+template <int G, bool kFused, int kW>
+__global__ void __launch_bounds__(Shape8<kW>::kWarps * 32, 1)
     decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const Int8Params p)
 {
+    using S = Shape8<kW>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -298,17 +343,17 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
 
     allow_dependent_launch();
-    unsigned char *stages = smem + warp * kStages8 * kStage8;
-    float *scales = reinterpret_cast<float *>(smem + kScaleOffset8) + warp * kStages8 * 2 * kChunkTokens;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOffset8) + warp * kStages8;
-    int *stage_rows = reinterpret_cast<int *>(smem + kRowsOffset8) + warp * kStages8;
+    unsigned char *stages = smem + warp * S::kStages * kStage8;
+    float *scales = reinterpret_cast<float *>(smem + S::kScaleOffset) + warp * S::kStages * 2 * kChunkTokens;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset) + warp * S::kStages;
+    int *stage_rows = reinterpret_cast<int *>(smem + S::kRowsOffset) + warp * S::kStages;
     if (lane == 0) {
         if (warp == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
         }
 #pragma unroll
-        for (int s = 0; s < kStages8; ++s)
+        for (int s = 0; s < S::kStages; ++s)
             mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
@@ -316,9 +361,9 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     const int part_tokens = p.ppp * p.P;
     const int tok0 = part * part_tokens;
     const int32_t *table = p.block_table + static_cast<size_t>(b) * p.max_pages;
-    auto chunk_token = [&](int k) { return tok0 + (warp + k * kWarps8) * kChunkTokens; };
+    auto chunk_token = [&](int k) { return tok0 + (warp + k * S::kWarps) * kChunkTokens; };
     int T = p.context_lens[b];
-    if (T < 0 || T > p.max_pages * p.P) {
+    if (T < (kFused ? 1 : 0) || T > p.max_pages * p.P) {
         if (part == 0 && threadIdx.x == 0)
             raise_flag8(PGQA_DEVERR_BAD_CONTEXT);
         T = 0;
@@ -330,12 +375,13 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     }
     const int tok1 = min(T, tok0 + part_tokens);
     const int n_chunks = max(0, (tok1 - tok0 + kChunkTokens - 1) / kChunkTokens);
-    const int my_chunks = (n_chunks > warp) ? (n_chunks - 1 - warp) / kWarps8 + 1 : 0;
+    const int my_chunks = (n_chunks > warp) ? (n_chunks - 1 - warp) / S::kWarps + 1 : 0;
     __syncwarp();
 
     // the chunk holding position T-1 is written by the prologue this kernel
-    // may overlap: it is requested after griddepcontrol.wait
-    auto holds_new_token = [&](int k) { return chunk_token(k) + kChunkTokens > T - 1; };
+    // may overlap: it is requested after griddepcontrol.wait (the fused step
+    // patches the new row into shared memory itself instead)
+    auto holds_new_token = [&](int k) { return !kFused && chunk_token(k) + kChunkTokens > T - 1; };
     // Physical pages of this warp's chunks, 32 at a time: lane L caches the
     // entry of chunk 32*blk + L. Called by the whole (converged) warp.
     int tbl_blk = -1, tbl_val = -1;
@@ -349,17 +395,17 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     };
     auto issue = [&](int k, int phys, uint64_t policy) { // lane 0
         const int t = chunk_token(k);
-        uint64_t *bar = &bars[k % kStages8];
+        uint64_t *bar = &bars[k % S::kStages];
         if (phys < 0 || phys >= p.num_pages) {
             raise_flag8(PGQA_DEVERR_BAD_PAGE);
-            stage_rows[k % kStages8] = 0;
+            stage_rows[k % S::kStages] = 0;
             mbar_arrive(bar);
             return;
         }
-        stage_rows[k % kStages8] = min(kChunkTokens, tok1 - t);
+        stage_rows[k % S::kStages] = min(kChunkTokens, tok1 - t);
         const int row = (phys * p.Hkv + kvh) * p.P + (t % p.P);
-        unsigned char *dst = stages + (k % kStages8) * kStage8;
-        float *sdst = scales + (k % kStages8) * 2 * kChunkTokens;
+        unsigned char *dst = stages + (k % S::kStages) * kStage8;
+        float *sdst = scales + (k % S::kStages) * 2 * kChunkTokens;
         mbar_arrive_expect_tx(bar, kStage8 + kScaleBytes8);
         tma_load_2d(dst, &tmap_k, 0, row, bar, policy);
         tma_load_2d(dst + kTile8, &tmap_v, 0, row, bar, policy);
@@ -368,60 +414,164 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     };
 
     const uint64_t policy = l2_evict_first_policy();
-    const int first = min(kStages8, my_chunks);
-    int first_phys[kStages8];
+    const int first = min(S::kStages, my_chunks);
+    int first_phys[S::kStages];
 #pragma unroll
-    for (int k = 0; k < kStages8; ++k)
+    for (int k = 0; k < S::kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
     if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < kStages8; ++k)
-            if (k < first && !holds_new_token(k))
+        for (int k = 0; k < S::kStages; ++k)
+            if (k < first && k < S::template kPrewait<kFused> && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
+
+    // fused step: warps < G rotate the query heads; the warp owning the chunk
+    // of position T-1 quantizes and appends the new K and V rows. What no
+    // earlier kernel writes (gains, rotation, the append slot) is prepared
+    // before the wait.
+    const int pos = T - 1;
+    const bool has_q = kFused && T > 0 && warp < G;
+    int new_chunk = -1, new_phys = -1;
+    if (kFused && T > 0 && pos >= tok0 && pos < tok1) {
+        const int c_idx = (pos - tok0) / kChunkTokens;
+        if (c_idx % S::kWarps == warp) {
+            new_chunk = c_idx / S::kWarps;
+            new_phys = table[pos / p.P];
+        }
+    }
+    HeadRope rope;
+    float gain_q[4], gain_k[4];
+    if (has_q || new_chunk >= 0)
+        rope.init(pos, p.freqs);
+    if (has_q)
+        load_head(p.gamma_q, gain_q);
+    if (new_chunk >= 0)
+        load_head(p.gamma_k, gain_k);
+
     grid_dependency_wait();
+
+    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
+    const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
+    float xq[4], xk[4], xv[4];
+    if (has_q)
+        load_head(p.q_raw + (row0 + warp) * kHeadDim, xq);
+    if (new_chunk >= 0) {
+        load_head(p.k_new + krow, xk);
+        load_head(p.v_new + krow, xv);
+    }
     Int8Warp<G> st;
-    st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim);
+    if constexpr (!kFused)
+        st.init(p.q + row0 * kHeadDim);
     if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < kStages8; ++k)
-            if (k < first && holds_new_token(k))
+        for (int k = 0; k < S::kStages; ++k)
+            if (k < first && (k >= S::template kPrewait<kFused> || holds_new_token(k)))
                 issue(k, first_phys[k], policy);
     }
     __syncwarp();
 
+    // fused step: normalise and rotate q; once every warp has its query, the
+    // warp owning the new position normalises and rotates K, quantizes K (its
+    // bf16 rounding) and V, appends them and keeps the row in shared memory
+    // for the patch of its staged chunk.
+    unsigned char *patch = smem + S::kPatchOffset;
+    if constexpr (kFused) {
+        uint16_t *q_buf = reinterpret_cast<uint16_t *>(smem + S::kQBufOffset);
+        if (has_q) {
+            norm_rope_apply(xq, gain_q, p.eps, rope);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint16_t bits = f32_to_bf16_bits(xq[i]);
+                q_buf[warp * kHeadDim + lane + 32 * i] = bits;
+                if (part == 0 && p.q_out)
+                    p.q_out[(row0 + warp) * kHeadDim + lane + 32 * i] = bits;
+            }
+        }
+        __syncthreads();
+        st.init(q_buf);
+        if (new_chunk >= 0) {
+            int kc[4], vc[4];
+            norm_rope_apply(xk, gain_k, p.eps, rope);
+            round_head_bf16(xk);
+            const float ks = quantize_head_int8(xk, kc);
+            const float vs = quantize_head_int8(xv, vc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                patch[lane + 32 * i] = static_cast<unsigned char>(kc[i]);
+                patch[kHeadDim + lane + 32 * i] = static_cast<unsigned char>(vc[i]);
+            }
+            if (lane == 0) {
+                reinterpret_cast<float *>(patch + 2 * kHeadDim)[0] = ks;
+                reinterpret_cast<float *>(patch + 2 * kHeadDim)[1] = vs;
+            }
+            if (new_phys >= 0 && new_phys < p.num_pages) {
+                const size_t slot_row = (static_cast<size_t>(new_phys) * p.Hkv + kvh) * p.P + pos % p.P;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    p.k_cache8[slot_row * kHeadDim + lane + 32 * i] = static_cast<int8_t>(kc[i]);
+                    p.v_cache8[slot_row * kHeadDim + lane + 32 * i] = static_cast<int8_t>(vc[i]);
+                }
+                if (lane == 0) {
+                    p.k_scale_out[slot_row] = ks;
+                    p.v_scale_out[slot_row] = vs;
+                }
+            } else if (lane == 0) {
+                raise_flag8(PGQA_DEVERR_BAD_PAGE);
+            }
+            __syncwarp();
+        }
+    }
+
     bool ok = true;
     int k0 = 0;
     for (int nc; k0 < my_chunks; k0 += nc) {
-        nc = min(kGroup8, my_chunks - k0);
-        uint32_t stage_addr[kGroup8];
-        const float *scl[kGroup8];
-        int rows[kGroup8];
+        nc = min(S::kGroup, my_chunks - k0);
+        uint32_t stage_addr[S::kGroup];
+        const float *scl[S::kGroup];
+        int rows[S::kGroup];
 #pragma unroll
-        for (int c = 0; c < kGroup8; ++c) {
+        for (int c = 0; c < S::kGroup; ++c) {
             const int k = k0 + c;
-            stage_addr[c] = smem_addr(stages + (k % kStages8) * kStage8);
-            scl[c] = scales + (k % kStages8) * 2 * kChunkTokens;
+            stage_addr[c] = smem_addr(stages + (k % S::kStages) * kStage8);
+            scl[c] = scales + (k % S::kStages) * 2 * kChunkTokens;
             rows[c] = 0;
             if (c < nc) {
-                const bool landed = mbar_wait_bounded(&bars[k % kStages8], (k / kStages8) & 1);
+                const bool landed = mbar_wait_bounded(&bars[k % S::kStages], (k / S::kStages) & 1);
                 if (!__all_sync(0xFFFFFFFFu, landed))
                     ok = false;
-                rows[c] = stage_rows[k % kStages8];
+                rows[c] = stage_rows[k % S::kStages];
+                if (kFused && k == new_chunk && rows[c] > 0) {
+                    // the staged copy predates the append: put the new row in
+                    // (word w < 64 of the patch: bytes 4w..4w+3 of the K row,
+                    // then of the V row)
+                    const int r = pos % kChunkTokens;
+                    unsigned char *stage = stages + (k % S::kStages) * kStage8;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int w = lane + 32 * i, x = 4 * (w & 31);
+                        const int off = (w >> 5) * kTile8 + r * 128 + (((x >> 4) ^ (r & 7)) << 4) + (x & 15);
+                        *reinterpret_cast<uint32_t *>(stage + off) = reinterpret_cast<const uint32_t *>(patch)[w];
+                    }
+                    if (lane < 2)
+                        scales[(k % S::kStages) * 2 * kChunkTokens + lane * kChunkTokens + r] =
+                            reinterpret_cast<const float *>(patch + 2 * kHeadDim)[lane];
+                    __syncwarp();
+                }
             }
         }
         if (!ok)
             break;
-        if (nc == 3)
-            st.template fold<3>(stage_addr, scl, rows, p.scale_log2);
-        else if (nc == 2)
-            st.template fold<2>(stage_addr, scl, rows, p.scale_log2);
+        if (S::kGroup >= 3 && nc == 3)
+            st.template fold<(S::kGroup >= 3 ? 3 : 1)>(stage_addr, scl, rows, p.scale_log2);
+        else if (S::kGroup >= 2 && nc == 2)
+            st.template fold<(S::kGroup >= 2 ? 2 : 1)>(stage_addr, scl, rows, p.scale_log2);
         else
             st.template fold<1>(stage_addr, scl, rows, p.scale_log2);
         __syncwarp();
 #pragma unroll
-        for (int c = 0; c < kGroup8; ++c) {
-            const int k = k0 + c + kStages8;
+        for (int c = 0; c < S::kGroup; ++c) {
+            const int k = k0 + c + S::kStages;
             if (c < nc && k < my_chunks) {
                 const int phys = phys_of(k);
                 if (lane == 0) {
@@ -435,9 +585,9 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     if (!ok) {
         if (lane == 0)
             raise_flag8(PGQA_DEVERR_WAIT_TIMEOUT);
-        const int issued = min(my_chunks, k0 + kStages8);
+        const int issued = min(my_chunks, k0 + S::kStages);
         for (int kk = k0; kk < issued; ++kk)
-            (void)mbar_wait_bounded(&bars[kk % kStages8], (kk / kStages8) & 1);
+            (void)mbar_wait_bounded(&bars[kk % S::kStages], (kk / S::kStages) & 1);
         st.clear();
     }
     __syncwarp();
@@ -445,19 +595,18 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
     st.store_record(reinterpret_cast<float *>(stages));
     __syncthreads();
 
-    const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
-    for (int e = threadIdx.x; e < G * kHeadDim; e += kWarps8 * 32) {
+    for (int e = threadIdx.x; e < G * kHeadDim; e += S::kWarps * 32) {
         const int h = e / kHeadDim, d = e % kHeadDim;
         float M = kEmptyMax;
 #pragma unroll
-        for (int w = 0; w < kWarps8; ++w) {
-            const float *rec = reinterpret_cast<const float *>(smem + w * kStages8 * kStage8);
+        for (int w = 0; w < S::kWarps; ++w) {
+            const float *rec = reinterpret_cast<const float *>(smem + w * S::kStages * kStage8);
             M = fmaxf(M, rec[G * kHeadDim + h]);
         }
         float L = 0.f, O = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps8; ++w) {
-            const float *rec = reinterpret_cast<const float *>(smem + w * kStages8 * kStage8);
+        for (int w = 0; w < S::kWarps; ++w) {
+            const float *rec = reinterpret_cast<const float *>(smem + w * S::kStages * kStage8);
             const float wt = exp2f(rec[G * kHeadDim + h] - M);
             L = fmaf(rec[G * kHeadDim + G + h], wt, L);
             O = fmaf(rec[h * kHeadDim + d], wt, O);
@@ -478,6 +627,30 @@ __global__ void __launch_bounds__(kWarps8 * 32, 1)
             p.ws_acc[idx * kHeadDim + d] = O;
         }
     }
+    if (n_parts == 1 || !p.fused_merge)
+        return;
+
+    // Ticket: the CTA that finishes last for this (sequence, KV head) merges.
+    // The barrier orders every thread's partial-state stores before thread
+    // 0's release; its acquire (when last) orders the other CTAs' stores
+    // before the merge's loads, which the second barrier extends to all
+    // threads.
+    unsigned *ticket_slot = reinterpret_cast<unsigned *>(smem + S::kTicketOffset);
+    __syncthreads();
+    unsigned *ticket = p.tickets + static_cast<size_t>(b) * p.Hkv + kvh;
+    if (threadIdx.x == 0)
+        *ticket_slot = atomic_add_acq_rel_gpu(ticket, 1u);
+    __syncthreads();
+    if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
+        return;
+    const auto row_of = [&](int c) { return row0 + c; };
+    if (!merge_partitions_in_cta<G, S::kWarps * 32, kFusedMergeMax8>(
+            p.ws_m, p.ws_l, p.ws_acc, p.NP, n_parts, row_of, p.out_f32, p.out_bf16, smem,
+            reinterpret_cast<uint64_t *>(smem + S::kMergeBarOffset)) &&
+        threadIdx.x == 0)
+        raise_flag8(PGQA_DEVERR_WAIT_TIMEOUT); // the merge's copy never landed: outputs left alone
+    if (threadIdx.x == 0)
+        *ticket = 0u; // ready for the next call
 }
 
 using EncodeTiledFn8 = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -517,23 +690,44 @@ cudaError_t encode_int8_map(CUtensorMap *map, const void *base, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G>
+template <int G, bool kFused, int kW>
 cudaError_t launch_int8_t(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
                           cudaStream_t stream)
 {
+    using S = Shape8<kW>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
     if (dev >= 64 || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_int8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem8);
+        err = cudaFuncSetAttribute(decode_int8_kernel<G, kFused, kW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   S::kSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < 64)
             configured[dev] = true;
     }
-    return launch_pdl(decode_int8_kernel<G>, grid, dim3(kWarps8 * 32), kSmem8, stream, mk, mv, kp);
+    return launch_pdl(decode_int8_kernel<G, kFused, kW>, grid, dim3(S::kWarps * 32), S::kSmem, stream, mk, mv,
+                      kp);
+}
+
+template <int kW> bool merges_in_kernel(int G, int num_partitions)
+{
+    using S = Shape8<kW>;
+    return num_partitions <= kFusedMergeMax8 &&
+           static_cast<long>(G) * num_partitions * kHeadDim * 4 + S::kMergeScratch <= S::kStageArea;
+}
+
+template <int G>
+cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
+                          bool fused, bool deep, cudaStream_t stream)
+{
+    if (deep)
+        return fused ? launch_int8_t<G, true, 12>(mk, mv, kp, grid, stream)
+                     : launch_int8_t<G, false, 12>(mk, mv, kp, grid, stream);
+    return fused ? launch_int8_t<G, true, 9>(mk, mv, kp, grid, stream)
+                 : launch_int8_t<G, false, 9>(mk, mv, kp, grid, stream);
 }
 
 } // namespace
@@ -568,27 +762,48 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
+    if (a.fused) {
+        kp.q_raw = a.q_raw;
+        kp.k_new = a.k_new;
+        kp.v_new = a.v_new;
+        kp.gamma_q = a.gamma_q;
+        kp.gamma_k = a.gamma_k;
+        kp.k_cache8 = const_cast<int8_t *>(a.k_cache8);
+        kp.v_cache8 = const_cast<int8_t *>(a.v_cache8);
+        kp.k_scale_out = const_cast<float *>(a.k_scale);
+        kp.v_scale_out = const_cast<float *>(a.v_scale);
+        kp.q_out = a.q_out;
+        kp.eps = a.eps;
+        kp.freqs = make_rope_freqs(a.rope_theta);
+    }
+    // long partitions take the 12-warp shape (fold-bound), short ones 9 warps
+    const bool deep = static_cast<long>(a.pages_per_part) * a.page_size >= kDeepChunks8 * kChunkTokens;
+    kp.fused_merge = (deep ? merges_in_kernel<12>(G, a.num_partitions) : merges_in_kernel<9>(G, a.num_partitions))
+                         ? 1
+                         : 0;
     if (a.num_partitions > 1) {
         const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;
-        const auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+        const auto align256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
         char *ws = reinterpret_cast<char *>(a.ws);
+        kp.tickets = reinterpret_cast<unsigned *>(ws);
+        ws += decode_ticket_bytes(a.B, a.Hkv);
         kp.ws_m = reinterpret_cast<float *>(ws);
-        kp.ws_l = reinterpret_cast<float *>(ws + a256(n * sizeof(float)));
-        kp.ws_acc = reinterpret_cast<float *>(ws + 2 * a256(n * sizeof(float)));
+        kp.ws_l = reinterpret_cast<float *>(ws + align256(n * sizeof(float)));
+        kp.ws_acc = reinterpret_cast<float *>(ws + 2 * align256(n * sizeof(float)));
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
     switch (G) {
-    case 1: err = launch_int8_t<1>(mk, mv, kp, grid, stream); break;
-    case 2: err = launch_int8_t<2>(mk, mv, kp, grid, stream); break;
-    case 3: err = launch_int8_t<3>(mk, mv, kp, grid, stream); break;
-    case 4: err = launch_int8_t<4>(mk, mv, kp, grid, stream); break;
-    case 5: err = launch_int8_t<5>(mk, mv, kp, grid, stream); break;
-    case 6: err = launch_int8_t<6>(mk, mv, kp, grid, stream); break;
-    case 7: err = launch_int8_t<7>(mk, mv, kp, grid, stream); break;
-    case 8: err = launch_int8_t<8>(mk, mv, kp, grid, stream); break;
+    case 1: err = launch_int8_g<1>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 2: err = launch_int8_g<2>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 3: err = launch_int8_g<3>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 4: err = launch_int8_g<4>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 5: err = launch_int8_g<5>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 6: err = launch_int8_g<6>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 7: err = launch_int8_g<7>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 8: err = launch_int8_g<8>(mk, mv, kp, grid, a.fused, deep, stream); break;
     default: return cudaErrorInvalidValue;
     }
-    if (err != cudaSuccess || a.num_partitions <= 1)
+    if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)
         return err;
     MergeArgs ma{};
     ma.m = kp.ws_m;
@@ -606,13 +821,12 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     return launch_merge(ma, stream);
 }
 
-size_t decode_int8_workspace_bytes(int B, int Hq, int num_partitions)
+// Same layout as the bf16 kernel's workspace: partition tickets [B*Hkv]
+// (zero before first use; every completed call leaves them zero), then m, l
+// [B*Hq*NP] and acc [B*Hq*NP*128].
+size_t decode_int8_workspace_bytes(int B, int Hkv, int Hq, int num_partitions)
 {
-    if (num_partitions <= 1)
-        return 0;
-    const size_t n = static_cast<size_t>(B) * Hq * num_partitions;
-    const auto a256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
-    return 2 * a256(n * sizeof(float)) + a256(n * kHeadDim * sizeof(float));
+    return decode_workspace_bytes(B, Hkv, Hq, num_partitions);
 }
 
 cudaError_t read_flags_int8(unsigned *flags, bool clear)

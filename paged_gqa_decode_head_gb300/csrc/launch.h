@@ -115,9 +115,16 @@ struct DecodeInt8Args {
     float *out_f32;
     pgqa_bf16 *out_bf16;
     float *ws;
+    // fused decode step (decode_step_paged_int8): the prologue runs in the
+    // attention kernel; q is unused, the caches are written
+    bool fused;
+    const pgqa_bf16 *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;
+    pgqa_bf16 *q_out;
+    double rope_theta;
+    float eps;
 };
 cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream);
-size_t decode_int8_workspace_bytes(int B, int Hq, int num_partitions);
+size_t decode_int8_workspace_bytes(int B, int Hkv, int Hq, int num_partitions);
 cudaError_t read_flags_int8(unsigned *flags, bool clear);
 
 // Launch `kernel` on `stream` with programmatic stream serialisation: it may

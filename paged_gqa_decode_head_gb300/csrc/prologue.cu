@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "head_norm_rope.cuh"
 #include "launch.h"
+#include "quantize_int8.cuh"
 
 namespace pgqa {
 namespace {
@@ -35,28 +36,6 @@ struct PrologueParams {
     float eps;
     RopeFreqs freqs;
 };
-
-// Symmetric per-row INT8 quantization of the head held by the warp (x[i] is
-// dim lane + 32 i): s = amax / 127, code = round_half_even(x / s), both in
-// binary32 with correctly rounded division (an all-zero row: s = 0, codes 0).
-__device__ __forceinline__ void store_row_int8(const float (&x)[4], int8_t *codes, float *scale)
-{
-    const int lane = threadIdx.x & 31;
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    const float s = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int c = 0;
-        if (amax > 0.0f)
-            c = max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], s))));
-        codes[lane + 32 * i] = static_cast<int8_t>(c);
-    }
-    if (lane == 0)
-        *scale = s;
-}
 
 template <bool kInt8>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const PrologueParams p)
@@ -119,12 +98,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) prologue_kernel(const Pro
     float x[4];
     norm_rope_head(src, gamma, p.eps, pos, p.freqs, x);
     if (kInt8 && !is_q) {
-        // quantize the bf16-rounded rotated K row
-        float xb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            xb[i] = bf16_bits_to_f32(f32_to_bf16_bits(x[i]));
-        store_row_int8(xb, p.k_cache8 + slot, p.k_scale + slot / kHeadDim);
+        round_head_bf16(x);
+        store_row_int8(x, p.k_cache8 + slot, p.k_scale + slot / kHeadDim);
         return;
     }
 #pragma unroll

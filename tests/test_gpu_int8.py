@@ -94,6 +94,41 @@ def test_int8_attention_group_sizes(Hq, Hkv):
     check_attention(kv, inputs.query(1141 + Hq, 2, Hq), 5)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (24, 8), (64, 8), (4, 1)])
+@pytest.mark.parametrize("num_partitions", [1, 2])
+def test_int8_attention_long_partitions(Hq, Hkv, num_partitions):
+    """Partitions of 64 chunks (1024 positions) or more run the 12-warp CTA
+    shape; a ragged tail and every group size on it."""
+    kv = inputs.paged_kv(1150 + Hq + num_partitions, [2000, 1100, 7], Hkv=Hkv, page_size=16, fill_unused="normal")
+    check_attention(kv, inputs.query(1150 + Hq, 3, Hq), num_partitions)
+
+
+@pytest.mark.parametrize("Hq,num_partitions", [(16, 19), (16, 64), (64, 60)])
+def test_int8_merge_paths_and_workspace_reuse(Hq, num_partitions):
+    """Up to 64 partitions whose states fit the stage area are merged by the
+    last CTA (16 heads at 19 and 64); 8 heads at 60 partitions do not fit and
+    go to the merge kernel. The same workspace serves repeated calls (the
+    ticket is left at zero) with identical results."""
+    ctx = [3000, 64 * 16 + 3, 40]
+    kv = inputs.paged_kv(1210 + num_partitions, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    q = inputs.query(1210 + num_partitions, len(ctx), Hq)
+    k8, v8, ks, vs = int8_cache(kv)
+    B = len(ctx)
+    n = pg.decode_attn_int8_workspace_size(B, Hq, 8, 128, kv.page_size, kv.max_pages, num_partitions)
+    ws = torch.zeros(max(16, n), dtype=torch.uint8, device="cuda")
+    args = (to_device_bf16(q, "cuda"), dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs),
+            to_device_i32(kv.block_table, "cuda"), to_device_i32(kv.context_lens, "cuda"), SCALE)
+    outs = []
+    for _ in range(3):
+        of = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        pg.decode_attn_paged_int8(*args, out_f32=of, workspace=ws, num_partitions=num_partitions)
+        outs.append(of.cpu().numpy())
+    ref = oracle.decode_attention_int8(q, k8, v8, ks, vs, kv.block_table, kv.context_lens, SCALE)
+    assert np.abs(outs[0] - ref).max() <= ATOL_F32
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    assert pg.device_error_flags() == 0
+
+
 @pytest.mark.parametrize("P", [32, 256])
 def test_int8_attention_page_sizes(P):
     kv = inputs.paged_kv(1160 + P, [1000, 3 * P + 2], Hkv=8, page_size=P, fill_unused="normal")
@@ -185,3 +220,90 @@ def test_int8_quality_gate_against_bf16_attention():
     print(f"INT8 vs bf16 attention: RMS relative {rms:.4f}, max abs {np.abs(of - ref).max():.4f}")
     assert rms <= 0.02
     assert np.abs(of - ref).max() <= 0.05
+
+
+def _fused_vs_two_launch(seed, ctx, Hq, num_partitions, page_size=16):
+    """Runs decode_step_paged_int8 and the prologue + attention pair on copies
+    of the same INT8 cache; returns both results and the oracle inputs."""
+    B, Hkv = len(ctx), 8
+    kv = inputs.paged_kv(seed, ctx, Hkv=Hkv, page_size=page_size, fill_unused="normal")
+    tok = inputs.new_token(seed, B, Hq, Hkv)
+    k8, v8, ks, vs = (np.nan_to_num(a) for a in int8_cache(kv))
+    dev = "cuda"
+    bt, cl = to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev)
+    raw = [to_device_bf16(a, dev) for a in (tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k)]
+    n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, page_size, kv.max_pages, num_partitions)
+    res = {}
+    for mode in ("fused", "two"):
+        cache = [dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs)]
+        ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+        q_out = torch.full((B, Hq, 128), 0x7FC0, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        of = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+        ob = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+        if mode == "fused":
+            pg.decode_step_paged_int8(*raw, cl, bt, *cache, SCALE, THETA, q_out=q_out, out_f32=of, out_bf16=ob,
+                                      workspace=ws, num_partitions=num_partitions)
+        else:
+            pg.qk_norm_rope_append_int8(*raw, cl, bt, *cache, q_out, THETA)
+            pg.decode_attn_paged_int8(q_out, *cache, bt, cl, SCALE, out_f32=of, out_bf16=ob, workspace=ws,
+                                      num_partitions=num_partitions)
+        torch.cuda.synchronize()
+        res[mode] = [t.cpu().numpy() for t in cache] + [bf16_bits(q_out), of.cpu().numpy(), bf16_bits(ob)]
+    return res, kv, tok, (k8, v8, ks, vs)
+
+
+@pytest.mark.parametrize("ctx,Hq,num_partitions", [
+    ([1, 16, 17, 300], 16, 0),
+    ([2049, 40, 8000], 16, 0),
+    ([2049, 40, 8000], 16, 70),
+    ([700, 1], 64, 5),
+    ([512, 513], 8, 1),
+])
+def test_int8_fused_step_equals_two_launches(ctx, Hq, num_partitions):
+    """decode_step_paged_int8 writes the same codes and scales, the same
+    rotated query and the same outputs (bit for bit) as the quantizing
+    prologue followed by the INT8 attention."""
+    res, *_ = _fused_vs_two_launch(1300 + sum(ctx) % 97 + Hq, ctx, Hq, num_partitions)
+    for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
+        assert np.array_equal(a, b, equal_nan=False), name
+    assert pg.device_error_flags() == 0
+
+
+@pytest.mark.parametrize("num_partitions", [0, 3])
+def test_int8_fused_step_matches_the_oracle(num_partitions):
+    ctx = [300, 17, 2049, 1]
+    res, kv, tok, (k8, v8, ks, vs) = _fused_vs_two_launch(1320 + num_partitions, ctx, 16, num_partitions)
+    q_ref, k8r, v8r, ksr, vsr = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, THETA)
+    ref = oracle.decode_attention_int8(q_ref, k8r, v8r, ksr, vsr, kv.block_table, kv.context_lens, SCALE)
+    gk8, gv8, gks, gvs, gq, of, ob = res["fused"]
+    assert np.abs(of - ref).max() <= ATOL_F32
+    assert_bf16_close(gq, q_ref, "q_out")
+    assert np.array_equal(gv8, v8r) and np.array_equal(gvs, vsr)
+    own = oracle.decode_attention_int8(gq, gk8, gv8, gks, gvs, kv.block_table, kv.context_lens, SCALE)
+    assert_bf16_close(ob, oracle.round_bf16(own), "out_bf16")
+    assert pg.device_error_flags() == 0
+
+
+def test_int8_fused_step_flags_empty_context_and_bad_page():
+    """T = 0 cannot hold the new token: zeros and the context flag. A new
+    position whose page lies outside the pool is not written: page flag."""
+    kv = inputs.paged_kv(1330, [40, 40], Hkv=8, page_size=16, fill_unused="normal")
+    kv.context_lens[0] = 0
+    kv.block_table[1, 2] = kv.num_pages + 9  # the page of position 39
+    tok = inputs.new_token(1330, 2, 16, 8)
+    k8, v8, ks, vs = (np.nan_to_num(a) for a in int8_cache(kv))
+    dev = "cuda"
+    cache = [dev_i8(k8), dev_i8(v8), dev_f32(ks), dev_f32(vs)]
+    n = pg.decode_attn_int8_workspace_size(2, 16, 8, 128, 16, kv.max_pages, 0)
+    ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+    of = torch.full((2, 16, 128), float("nan"), dtype=torch.float32, device=dev)
+    raw = [to_device_bf16(a, dev) for a in (tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k)]
+    pg.decode_step_paged_int8(*raw, to_device_i32(kv.context_lens, dev), to_device_i32(kv.block_table, dev), *cache,
+                              SCALE, THETA, out_f32=of, workspace=ws)
+    flags = pg.device_error_flags()
+    assert flags & binding.DEVERR_BAD_CONTEXT and flags & binding.DEVERR_BAD_PAGE
+    out = of.cpu().numpy()
+    assert np.all(out[0] == 0) and np.isfinite(out).all()
+    assert np.array_equal(cache[0].cpu().numpy(), k8) and np.array_equal(cache[2].cpu().numpy(), ks)

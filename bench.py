@@ -238,6 +238,7 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ GPU leg
 def run_ours(args, rank, world, local):
+    import numpy as np
     import torch
 
     import paged_gqa_decode_head_gb300 as pg
@@ -325,23 +326,20 @@ def run_ours(args, rank, world, local):
     t_wall2 = time.time()
 
     # end to end through the public API: per step the new tokens (q, k, v of
-    # every layer) come from pinned host memory and the outputs go back.
-    host_in = []
-    for kv, tok in layers:
-        host_in.append([torch.from_numpy(a.view("int16")).view(torch.bfloat16).pin_memory()
-                        for a in (tok.q, tok.k, tok.v)])
-    host_out = [torch.empty(st.out_f32.shape, dtype=torch.float32).pin_memory() for st in step.layers]
-    h2d = sum(t.numel() * 2 for trio in host_in for t in trio)
-    d2h = sum(t.numel() * 4 for t in host_out)
+    # every layer, packed as the step's new_tokens buffer) come from pinned
+    # host memory in one copy and the fp32 outputs of every layer go back in
+    # one copy.
+    host_in = torch.cat([torch.from_numpy(np.concatenate([a.reshape(-1).view("int16") for a in (tok.q, tok.k, tok.v)]))
+                         for _, tok in layers]).view(torch.bfloat16).pin_memory()
+    host_out = torch.empty(step.outputs.shape, dtype=torch.float32).pin_memory()
+    assert host_in.numel() == step.new_tokens.numel()
+    h2d = host_in.numel() * 2
+    d2h = host_out.numel() * 4
 
     def e2e_step():
-        for trio, st in zip(host_in, step.layers):
-            st.q.copy_(trio[0], non_blocking=True)
-            st.k.copy_(trio[1], non_blocking=True)
-            st.v.copy_(trio[2], non_blocking=True)
+        step.new_tokens.copy_(host_in, non_blocking=True)
         step_graph.replay()
-        for ho, st in zip(host_out, step.layers):
-            ho.copy_(st.out_f32, non_blocking=True)
+        host_out.copy_(step.outputs, non_blocking=True)
 
     for _ in range(3):
         e2e_step()

@@ -66,20 +66,36 @@ class DecodeStep:
         self.scale = float(scale) if scale is not None else 1.0 / math.sqrt(self.D)
         self.layers: list[LayerState] = []
         ws_bytes = 0
-        for kv, tok in layers:
-            B = int(kv.context_lens.shape[0])
+        # Every layer's new-token heads (q, k, v) live in one buffer and every
+        # layer's fp32 output in another, so a step's inputs and results move
+        # between host and device in one copy each (``new_tokens``,
+        # ``outputs``); the per-layer tensors are views into them.
+        B = int(layers[0][0].context_lens.shape[0]) if layers else 0
+        if any(int(kv.context_lens.shape[0]) != B for kv, _ in layers):
+            raise ValueError("every layer of a decode step has the same batch")
+        q_n, kv_n = B * Hq * self.D, B * Hkv * self.D
+        per_layer = q_n + 2 * kv_n
+        self.new_tokens = torch.empty(len(layers) * per_layer, dtype=torch.bfloat16, device=self.device)
+        self.outputs = torch.empty((len(layers), B, Hq, self.D), dtype=torch.float32, device=self.device)
+        for i, (kv, tok) in enumerate(layers):
+            heads = self.new_tokens[i * per_layer:(i + 1) * per_layer]
+            q, k, v = (heads[:q_n].view(B, Hq, self.D), heads[q_n:q_n + kv_n].view(B, Hkv, self.D),
+                       heads[q_n + kv_n:].view(B, Hkv, self.D))
+            q.copy_(to_device_bf16(tok.q, self.device))
+            k.copy_(to_device_bf16(tok.k, self.device))
+            v.copy_(to_device_bf16(tok.v, self.device))
             st = LayerState(
                 k_cache=to_device_bf16(kv.k_cache, self.device),
                 v_cache=to_device_bf16(kv.v_cache, self.device),
                 block_table=to_device_i32(kv.block_table, self.device),
                 context_lens=to_device_i32(kv.context_lens, self.device),
-                q=to_device_bf16(tok.q, self.device),
-                k=to_device_bf16(tok.k, self.device),
-                v=to_device_bf16(tok.v, self.device),
+                q=q,
+                k=k,
+                v=v,
                 gamma_q=to_device_bf16(tok.gamma_q, self.device),
                 gamma_k=to_device_bf16(tok.gamma_k, self.device),
                 q_out=torch.empty((B, Hq, self.D), dtype=torch.bfloat16, device=self.device),
-                out_f32=torch.empty((B, Hq, self.D), dtype=torch.float32, device=self.device),
+                out_f32=self.outputs[i],
                 out_bf16=torch.empty((B, Hq, self.D), dtype=torch.bfloat16, device=self.device),
                 page_size=kv.page_size,
             )

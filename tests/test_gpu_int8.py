@@ -307,3 +307,22 @@ def test_int8_fused_step_flags_empty_context_and_bad_page():
     out = of.cpu().numpy()
     assert np.all(out[0] == 0) and np.isfinite(out).all()
     assert np.array_equal(cache[0].cpu().numpy(), k8) and np.array_equal(cache[2].cpu().numpy(), ks)
+
+
+def test_int8_fused_step_full_size_t8192():
+    """One layer of the Qwen3-0.6B-shaped step (B = 1, Hq = 16, Hkv = 8,
+    T = 8192, P = 16) over an INT8 cache, in the launch configuration the
+    benchmark times (automatic partition count), against the oracle's INT8
+    prologue and attention on every output."""
+    res, kv, tok, (k8, v8, ks, vs) = _fused_vs_two_launch(1340, [8192], 16, 0)
+    q_ref, k8r, v8r, ksr, vsr = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, THETA)
+    ref = oracle.decode_attention_int8(q_ref, k8r, v8r, ksr, vsr, kv.block_table, kv.context_lens, SCALE)
+    gk8, gv8, gks, gvs, gq, of, ob = res["fused"]
+    assert np.abs(of - ref).max() <= ATOL_F32
+    own = oracle.decode_attention_int8(gq, gk8, gv8, gks, gvs, kv.block_table, kv.context_lens, SCALE)
+    assert_bf16_close(ob, oracle.round_bf16(own), "out_bf16")
+    for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
+        assert np.array_equal(a, b), name
+    assert pg.device_error_flags() == 0

@@ -613,19 +613,26 @@ def run_secondary(args):
     qd = to_device_bf16(q, dev)
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
     n_slots = 2
-    slots_k = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
-    slots_v = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
-    events = [torch.cuda.Event() for _ in range(2 * n_slots)]
     m = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     l = torch.empty_like(m)
     acc = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
     copy_stream = torch.cuda.Stream(dev)
-    s = timed(lambda: pg.attn_host_tiled_run(qd, hk, hv, scale, slots_k, slots_v, events, m, l, acc, out_f32=out,
-                                             tile_len=tile, copy_stream=copy_stream))
     cfg = {"B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "host_bytes": nbytes,
            "link_probe": "256 MiB pinned host-to-device cudaMemcpyAsync, best of 3"}
-    emit(f"attn_host_tiled_run ({tile}-position tiles, {n_slots} slots)", nbytes, s, link, "GB/s", "measured link",
-         {"config": cfg})
+    # one tile per copy (the pages' pipeline), then eight 512-position tiles
+    # per copy (8 MiB transfers), each tile still updated on its own
+    for per_copy in (1, 8):
+        slots_k = [torch.empty((B, tile * per_copy, Hkv, 128), dtype=torch.bfloat16, device=dev)
+                   for _ in range(n_slots)]
+        slots_v = [torch.empty((B, tile * per_copy, Hkv, 128), dtype=torch.bfloat16, device=dev)
+                   for _ in range(n_slots)]
+        events = [torch.cuda.Event() for _ in range(2 * n_slots)]
+        s = timed(lambda: pg.attn_host_tiled_run(qd, hk, hv, scale, slots_k, slots_v, events, m, l, acc,
+                                                 out_f32=out, tile_len=tile, tiles_per_copy=per_copy,
+                                                 copy_stream=copy_stream))
+        emit(f"attn_host_tiled_run ({tile}-position tiles, {per_copy} per copy, {n_slots} slots)", nbytes, s, link,
+             "GB/s", "measured link", {"config": cfg})
+        del slots_k, slots_v
     n = pg.attn_host_direct_workspace_size(B, Hq, Hkv, T, 0)
     ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
     np_used = pg.attn_host_direct_partition_count(B, Hkv, T, 0)

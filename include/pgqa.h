@@ -352,27 +352,33 @@ int attn_tile_finalize(const float *m, const float *l, const float *acc, int B, 
 
 /*
  * attn_host_tiled_run -- enqueue the whole host-tiled attention: init, then
- * for each tile t of tile_len positions (the last may be shorter) a copy of
- * K and V from pinned host memory into device slot s = t % n_slots on
- * copy_stream, then attn_tile_update on compute_stream, then finalize.
- * Two event dependencies per slot order the slots (copy_done[s]: data ready
- * before it is read; compute_done[s]: slot free before it is overwritten),
- * so copies of later tiles overlap the update of earlier ones.
+ * for each group g of tiles_per_copy consecutive tiles of tile_len positions
+ * (the last group and tile may be shorter) one copy of K and one of V from
+ * pinned host memory into device slot s = g % n_slots on copy_stream, then
+ * attn_tile_update for each of the group's tiles in order on
+ * compute_stream, then finalize. Two event dependencies per slot order the
+ * slots (copy_done[s]: data ready before it is read; compute_done[s]: slot
+ * free before it is overwritten), so copies of later tiles overlap the
+ * updates of earlier ones. tiles_per_copy = 1 is the one-tile-per-copy
+ * pipeline of [EdgeTransformerEngine]'s KV-offload design; larger groups
+ * keep its 512-position tile updates and state but move the data in fewer,
+ * larger copies, which the host link serves faster.
  *
  *   host_k, host_v  [B][T][Hkv][D] bf16, pinned host memory
  *   k_slots, v_slots  host arrays of n_slots device pointers, each slot
- *                     [B][tile_len][Hkv][D] bf16; 2 <= n_slots <= 8
+ *                     [B][tiles_per_copy * tile_len][Hkv][D] bf16;
+ *                     2 <= n_slots <= 8
  *   events          host array of 2 * n_slots caller-created events
  *                   (copy_done[0..n_slots), then compute_done[0..n_slots))
- *   tile_len        1..512
+ *   tile_len        1..512;  tiles_per_copy  1..64
  * Returns after enqueueing; the output is ready when compute_stream reaches
  * the end of the enqueued work. The streams must differ.
  */
 int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
                         int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
-                        int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
-                        cudaEvent_t const *events, float *m, float *l, float *acc,
-                        float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
+                        int tiles_per_copy, int n_slots, pgqa_bf16 *const *k_slots,
+                        pgqa_bf16 *const *v_slots, cudaEvent_t const *events, float *m, float *l,
+                        float *acc, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
                         cudaStream_t copy_stream);
 
 /*

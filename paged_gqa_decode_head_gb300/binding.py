@@ -121,7 +121,7 @@ def load_library():
         lib.attn_tile_update.restype = I
         lib.attn_tile_finalize.argtypes = [P, P, P, I, I, I, P, P, P]
         lib.attn_tile_finalize.restype = I
-        lib.attn_host_tiled_run.argtypes = [P, P, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P, P, P, P]
+        lib.attn_host_tiled_run.argtypes = [P, P, P, I, I, I, I, I, F, I, I, I, P, P, P, P, P, P, P, P, P, P]
         lib.attn_host_tiled_run.restype = I
         lib.attn_host_direct_partition_count.argtypes = [I, I, I, I]
         lib.attn_host_direct_partition_count.restype = I
@@ -413,9 +413,10 @@ def attn_tile_finalize(m, l, acc, out_f32=None, out_bf16=None, stream=None) -> N
 
 
 def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, events, m, l, acc, out_f32=None,
-                        out_bf16=None, tile_len: int = 512, compute_stream=None, copy_stream=None) -> None:
+                        out_bf16=None, tile_len: int = 512, tiles_per_copy: int = 1, compute_stream=None,
+                        copy_stream=None) -> None:
     """host_k/host_v: pinned CPU bf16 [B, T, Hkv, D]; k_slots/v_slots: lists of device
-    [B, tile_len, Hkv, D] buffers; events: 2*len(k_slots) torch.cuda.Event objects."""
+    [B, tiles_per_copy * tile_len, Hkv, D] buffers; events: 2*len(k_slots) torch.cuda.Event objects."""
     lib = load_library()
     bf, f32 = torch.bfloat16, torch.float32
     B, Hq, D = q.shape
@@ -433,7 +434,7 @@ def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, event
         raise ValueError("copy_stream is required (a stream other than the compute stream)")
     st = lib.attn_host_tiled_run(
         _dev(q, bf, "q"), _host(host_k, bf, "host_k"), _host(host_v, bf, "host_v"), T, B, Hq, Hkv, D, float(scale),
-        int(tile_len), n, ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p),
+        int(tile_len), int(tiles_per_copy), n, ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p),
         ctypes.cast(ep, ctypes.c_void_p), _dev(m, f32, "m"), _dev(l, f32, "l"), _dev(acc, f32, "acc"),
         _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
         _stream(compute_stream), _stream(copy_stream))

@@ -476,7 +476,7 @@ int attn_tile_update(const pgqa_bf16 *q, const pgqa_bf16 *k_tile, const pgqa_bf1
     if (!aligned16(q) || !aligned16(k_tile) || !aligned16(v_tile) || !aligned4(m) || !aligned4(l) ||
         !aligned16(acc))
         return fail(PGQA_ERR_MISALIGNED, "%s: tensors need 16-byte, m/l 4-byte alignment", fn);
-    pgqa::TileArgs a{q, k_tile, v_tile, n_pos, B, Hq, Hkv, scale, m, l, acc};
+    pgqa::TileArgs a{q, k_tile, v_tile, n_pos, B, Hq, Hkv, scale, m, l, acc, n_pos};
     cudaError_t err = pgqa::launch_tile_update(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
@@ -506,16 +506,18 @@ int attn_tile_finalize(const float *m, const float *l, const float *acc, int B, 
 
 int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
                         int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
-                        int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
-                        cudaEvent_t const *events, float *m, float *l, float *acc,
-                        float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
+                        int tiles_per_copy, int n_slots, pgqa_bf16 *const *k_slots,
+                        pgqa_bf16 *const *v_slots, cudaEvent_t const *events, float *m, float *l,
+                        float *acc, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
                         cudaStream_t copy_stream)
 {
     const char *fn = "attn_host_tiled_run";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
-    if (T < 0 || tile_len < 1 || tile_len > 512 || n_slots < 2 || n_slots > 8)
-        return fail(PGQA_ERR_INVALID_ARG, "%s: need T >= 0, tile_len in [1, 512], n_slots in [2, 8]", fn);
+    if (T < 0 || tile_len < 1 || tile_len > 512 || n_slots < 2 || n_slots > 8 || tiles_per_copy < 1 ||
+        tiles_per_copy > 64)
+        return fail(PGQA_ERR_INVALID_ARG,
+                    "%s: need T >= 0, tile_len in [1, 512], tiles_per_copy in [1, 64], n_slots in [2, 8]", fn);
     if (compute_stream == copy_stream)
         return fail(PGQA_ERR_INVALID_ARG, "%s: compute and copy streams must differ", fn);
     if (B == 0)
@@ -544,17 +546,21 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
         (err = cudaStreamWaitEvent(copy_stream, compute_done[0], 0)) != cudaSuccess)
         return cuda_fail(err, "attn_host_tiled_run: initial stream ordering");
     const size_t pos_bytes = static_cast<size_t>(Hkv) * D * sizeof(pgqa_bf16);
-    const int n_tiles = (T + tile_len - 1) / tile_len;
-    for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % n_slots;
-        const int t0 = t * tile_len;
-        const int n_pos = T - t0 < tile_len ? T - t0 : tile_len;
-        // The slot is free once the update that last read it has finished.
-        if (t >= n_slots && (err = cudaStreamWaitEvent(copy_stream, compute_done[s], 0)) != cudaSuccess)
+    // A copy fills a slot with up to tiles_per_copy consecutive tiles (one
+    // transfer per slot and tensor: large copies reach the link's rate, 1 MiB
+    // ones about half of it); the tiles are then updated one at a time.
+    const long span_len = static_cast<long>(tiles_per_copy) * tile_len;
+    const long n_copies = (static_cast<long>(T) + span_len - 1) / span_len;
+    for (long g = 0; g < n_copies; ++g) {
+        const int s = static_cast<int>(g % n_slots);
+        const int t0 = static_cast<int>(g * span_len);
+        const int n_span = T - t0 < span_len ? T - t0 : static_cast<int>(span_len);
+        // The slot is free once the updates that last read it have finished.
+        if (g >= n_slots && (err = cudaStreamWaitEvent(copy_stream, compute_done[s], 0)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(copy)");
-        // Host rows of sequence b are [b][t0 .. t0+n_pos); the slot holds
-        // [b][0 .. n_pos) packed: a 2-D copy with one row per sequence.
-        const size_t row_bytes = static_cast<size_t>(n_pos) * pos_bytes;
+        // Host rows of sequence b are [b][t0 .. t0+n_span); the slot holds
+        // [b][0 .. n_span) packed: a 2-D copy with one row per sequence.
+        const size_t row_bytes = static_cast<size_t>(n_span) * pos_bytes;
         const size_t src_pitch = static_cast<size_t>(T) * pos_bytes;
         const size_t dst_pitch = row_bytes;
         const char *hk = reinterpret_cast<const char *>(host_k) + static_cast<size_t>(t0) * pos_bytes;
@@ -576,10 +582,13 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
             return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(copy)");
         if ((err = cudaStreamWaitEvent(compute_stream, copy_done[s], 0)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(compute)");
-        st = attn_tile_update(q, k_slots[s], v_slots[s], n_pos, B, Hq, Hkv, D, scale, m, l, acc,
-                              compute_stream);
-        if (st != PGQA_OK)
-            return st;
+        for (int p0 = 0; p0 < n_span; p0 += tile_len) {
+            const size_t off = static_cast<size_t>(p0) * Hkv * D;
+            pgqa::TileArgs a{q, k_slots[s] + off, v_slots[s] + off, n_span - p0 < tile_len ? n_span - p0 : tile_len,
+                             B, Hq, Hkv, scale, m, l, acc, n_span};
+            if ((err = pgqa::launch_tile_update(a, compute_stream)) != cudaSuccess)
+                return cuda_fail(err, "attn_host_tiled_run: tile update");
+        }
         if ((err = cudaEventRecord(compute_done[s], compute_stream)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(compute)");
     }

@@ -45,6 +45,7 @@
 #include "head_norm_rope.cuh"
 #include "launch.h"
 #include "partition_merge.cuh"
+#include "tensor_map.h"
 
 namespace pgqa {
 namespace {
@@ -843,26 +844,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
 constexpr int kMaxDevices = 64;
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
 // A paged cache seen as a 3-D tensor [2 halves][num_pages * Hkv * P rows]
 // [64 bf16]: element (x, row, half) is column 64*half + x of that row. One
 // box {64, 16, 2} is a whole 16-row chunk, landing in shared memory as the
@@ -871,7 +852,7 @@ EncodeTiledFn encode_fn()
 // bank conflicts; one TMA instruction moves a 4 KiB chunk of K (or V).
 cudaError_t encode_cache_map(CUtensorMap *map, const void *base, long long rows)
 {
-    EncodeTiledFn fn = encode_fn();
+    EncodeTiledFn fn = tensor_map_encoder();
     if (!fn)
         return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {64u, static_cast<cuuint64_t>(rows), 2u};
@@ -977,6 +958,21 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
     np = std::min<long>(std::max<long>(np, 1), std::min(max_pages, kMaxPartitions));
     const long ppp = (max_pages + np - 1) / np;
     return static_cast<int>((max_pages + ppp - 1) / ppp);
+}
+
+EncodeTiledFn tensor_map_encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
 }
 
 size_t decode_ticket_bytes(int B, int Hkv)

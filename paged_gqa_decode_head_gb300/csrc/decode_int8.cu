@@ -32,7 +32,6 @@
 // shared memory.
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include <cuda.h>
 
@@ -41,6 +40,7 @@
 #include "launch.h"
 #include "partition_merge.cuh"
 #include "quantize_int8.cuh"
+#include "tensor_map.h"
 
 namespace pgqa {
 namespace {
@@ -653,31 +653,11 @@ __global__ void __launch_bounds__(Shape8<kW>::kWarps * 32, 1)
         *ticket = 0u; // ready for the next call
 }
 
-using EncodeTiledFn8 = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                    CUtensorMapFloatOOBfill);
-
-EncodeTiledFn8 encode_fn8()
-{
-    static EncodeTiledFn8 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn8>(ptr);
-    });
-    return fn;
-}
-
 // An INT8 cache as a 2-D tensor [rows][128 bytes]; one box {128, 16} is a
 // 16-row tile with 128-byte swizzle.
 cudaError_t encode_int8_map(CUtensorMap *map, const void *base, long long rows)
 {
-    EncodeTiledFn8 fn = encode_fn8();
+    EncodeTiledFn fn = tensor_map_encoder();
     if (!fn)
         return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(rows)};

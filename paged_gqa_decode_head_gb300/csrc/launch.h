@@ -62,6 +62,7 @@ struct TileArgs {
     int n_pos, B, Hq, Hkv;
     float scale;
     float *m, *l, *acc;
+    int seq_stride; // positions from one sequence's rows to the next's in the tile buffers (0: n_pos)
 };
 
 struct HostDirectArgs {

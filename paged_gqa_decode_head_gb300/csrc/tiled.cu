@@ -7,11 +7,16 @@
 // (m = -1e30, l = 0, acc = 0), a per-tile update that rescales the state in
 // place, and finalize (out = acc / l). Tiles hold 512 positions.
 //
-// The update kernel runs one CTA per (sequence, KV head) with 8 warps; each
-// warp folds 16-key chunks straight from the (L2-resident, just copied) tile
-// with 16-byte loads, the warps' states are merged in shared memory, and the
-// result is merged into the global state. m is stored in natural-log units.
+// The update kernel runs one thread-block cluster of kTileSplit CTAs per
+// (sequence, KV head), each CTA with 8 warps folding a contiguous share of
+// the tile's 16-key chunks straight from the (L2-resident, just copied) tile
+// with 16-byte loads. Each CTA merges its warps' states in shared memory;
+// then CTA 0 of the cluster reads the other CTAs' states through distributed
+// shared memory and merges them into the global state. m is stored in
+// natural-log units.
 #include <algorithm>
+
+#include <cooperative_groups.h>
 
 #include "attn_core.cuh"
 #include "launch.h"
@@ -20,6 +25,7 @@ namespace pgqa {
 namespace {
 
 constexpr int kTileWarps = 8;
+constexpr int kTileSplit = 8; // CTAs (one cluster) per (sequence, KV head) and tile
 
 __global__ void tile_init_kernel(float *m, float *l, float *acc, int rows)
 {
@@ -39,29 +45,35 @@ __global__ void tile_init_kernel(float *m, float *l, float *acc, int rows)
 struct TileParams {
     const __nv_bfloat16 *q;
     const char *k_tile, *v_tile;
-    int n_pos, Hq, Hkv;
+    int n_pos, seq_stride, Hq, Hkv;
     float scale_log2;
     float *m, *l, *acc;
 };
 
 template <int G>
-__global__ void __launch_bounds__(kTileWarps * 32) tile_update_kernel(const TileParams p)
+__global__ void __cluster_dims__(kTileSplit, 1, 1) __launch_bounds__(kTileWarps * 32)
+    tile_update_kernel(const TileParams p)
 {
     constexpr int kRec = record_floats<G>();
     constexpr int kPerThread = (G * kHeadDim + kTileWarps * 32 - 1) / (kTileWarps * 32);
     __shared__ __align__(16) float recs[kTileWarps][kRec];
+    __shared__ __align__(16) float cta_rec[kRec]; // this CTA's state, read by CTA 0 of the cluster
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
     const int warp = threadIdx.x >> 5;
-    const int kvh = blockIdx.x;
-    const int b = blockIdx.y;
+    const int rank = blockIdx.x; // the cluster spans gridDim.x = kTileSplit
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
 
     allow_dependent_launch();
     grid_dependency_wait();
     WarpAttn<G> st;
     st.init(p.q + (static_cast<size_t>(b) * p.Hq + kvh * G) * kHeadDim, p.scale_log2);
     const long stride = static_cast<long>(p.Hkv) * kRowBytes; // one position, all KV heads
-    const size_t base = (static_cast<size_t>(b) * p.n_pos * p.Hkv + kvh) * kRowBytes;
+    const size_t base = (static_cast<size_t>(b) * p.seq_stride * p.Hkv + kvh) * kRowBytes;
     const int n_chunks = (p.n_pos + kChunkTokens - 1) / kChunkTokens;
-    for (int c = warp; c < n_chunks; c += kTileWarps) {
+    const int per_cta = (n_chunks + kTileSplit - 1) / kTileSplit;
+    const int c_end = min(n_chunks, (rank + 1) * per_cta);
+    for (int c = rank * per_cta + warp; c < c_end; c += kTileWarps) {
         const size_t off = base + static_cast<size_t>(c) * kChunkTokens * stride;
         st.fold_chunk(GlobalRows{p.k_tile + off, p.v_tile + off, stride},
                       min(kChunkTokens, p.n_pos - c * kChunkTokens));
@@ -70,44 +82,70 @@ __global__ void __launch_bounds__(kTileWarps * 32) tile_update_kernel(const Tile
     st.store_record(recs[warp]);
     __syncthreads();
 
-    float newM[kPerThread], newL[kPerThread], newO[kPerThread];
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        const int e = threadIdx.x + i * kTileWarps * 32;
-        if (e >= G * kHeadDim)
-            break;
+    // this CTA's state (base-2 m; warps without chunks hold m = -1e30, l = 0)
+    for (int e = threadIdx.x; e < G * kHeadDim; e += kTileWarps * 32) {
         const int h = e / kHeadDim, d = e % kHeadDim;
-        const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + h;
-        const float m_old = p.m[row] * kLog2e;
-        float M = m_old;
+        float M = kEmptyMax;
 #pragma unroll
         for (int w = 0; w < kTileWarps; ++w)
             M = fmaxf(M, recs[w][G * kHeadDim + h]);
-        const float w_old = exp2f(m_old - M);
-        float L = p.l[row] * w_old;
-        float O = p.acc[row * kHeadDim + d] * w_old;
+        float L = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kTileWarps; ++w) {
             const float wt = exp2f(recs[w][G * kHeadDim + h] - M);
             L = fmaf(recs[w][G * kHeadDim + G + h], wt, L);
             O = fmaf(recs[w][h * kHeadDim + d], wt, O);
         }
-        newM[i] = M, newL[i] = L, newO[i] = O;
-    }
-    __syncthreads(); // every thread has read the old (m, l) before any is replaced
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        const int e = threadIdx.x + i * kTileWarps * 32;
-        if (e >= G * kHeadDim)
-            break;
-        const int h = e / kHeadDim, d = e % kHeadDim;
-        const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + h;
-        p.acc[row * kHeadDim + d] = newO[i];
+        cta_rec[h * kHeadDim + d] = O;
         if (d == 0) {
-            p.m[row] = newM[i] * kLn2;
-            p.l[row] = newL[i];
+            cta_rec[G * kHeadDim + h] = M;
+            cta_rec[G * kHeadDim + G + h] = L;
         }
     }
+    cluster.sync(); // every CTA's state is complete and visible to the cluster
+
+    if (rank == 0) {
+        float newM[kPerThread], newL[kPerThread], newO[kPerThread];
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+            const int e = threadIdx.x + i * kTileWarps * 32;
+            if (e >= G * kHeadDim)
+                break;
+            const int h = e / kHeadDim, d = e % kHeadDim;
+            const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + h;
+            const float m_old = p.m[row] * kLog2e;
+            float M = m_old;
+#pragma unroll
+            for (int r = 0; r < kTileSplit; ++r)
+                M = fmaxf(M, cluster.map_shared_rank(cta_rec, r)[G * kHeadDim + h]);
+            const float w_old = exp2f(m_old - M);
+            float L = p.l[row] * w_old;
+            float O = p.acc[row * kHeadDim + d] * w_old;
+#pragma unroll
+            for (int r = 0; r < kTileSplit; ++r) {
+                const float *rec = cluster.map_shared_rank(cta_rec, r);
+                const float wt = exp2f(rec[G * kHeadDim + h] - M);
+                L = fmaf(rec[G * kHeadDim + G + h], wt, L);
+                O = fmaf(rec[h * kHeadDim + d], wt, O);
+            }
+            newM[i] = M, newL[i] = L, newO[i] = O;
+        }
+        __syncthreads(); // every thread has read the old (m, l) before any is replaced
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+            const int e = threadIdx.x + i * kTileWarps * 32;
+            if (e >= G * kHeadDim)
+                break;
+            const int h = e / kHeadDim, d = e % kHeadDim;
+            const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + h;
+            p.acc[row * kHeadDim + d] = newO[i];
+            if (d == 0) {
+                p.m[row] = newM[i] * kLn2;
+                p.l[row] = newL[i];
+            }
+        }
+    }
+    cluster.sync(); // the other CTAs keep their state until CTA 0 has read it
 }
 
 __global__ void tile_finalize_kernel(const float *l, const float *acc, int rows, float *out_f32,
@@ -227,13 +265,14 @@ cudaError_t launch_tile_update(const TileArgs &a, cudaStream_t stream)
     p.k_tile = reinterpret_cast<const char *>(a.k_tile);
     p.v_tile = reinterpret_cast<const char *>(a.v_tile);
     p.n_pos = a.n_pos;
+    p.seq_stride = a.seq_stride > 0 ? a.seq_stride : a.n_pos;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.scale_log2 = a.scale * kLog2e;
     p.m = a.m;
     p.l = a.l;
     p.acc = a.acc;
-    const dim3 grid(a.Hkv, a.B);
+    const dim3 grid(kTileSplit, a.Hkv, a.B);
     const int threads = kTileWarps * 32;
     const dim3 block(threads);
     switch (a.Hq / a.Hkv) {

@@ -104,8 +104,12 @@ def test_prologue_and_tile_validation(lib):
     assert lib.attn_tile_init(None, None, None, 1, 16, 64, None) == -2
     assert lib.attn_partition_merge(None, None, None, 1, 16, 128, 0, None, None, None) == -1
     assert lib.attn_partition_merge(None, None, None, 1, 16, 128, 70000, None, None, None) == -2
-    assert lib.attn_host_tiled_run(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 1,
+    assert lib.attn_host_tiled_run(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 1, 1,
                                    *([None] * 10)) == -1
+    assert lib.attn_host_tiled_run(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 0, 2,
+                                   *([None] * 10)) == -1  # tiles_per_copy < 1
+    assert lib.attn_host_tiled_run(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 65, 2,
+                                   *([None] * 10)) == -1  # tiles_per_copy > 64
     del P
 
 

@@ -92,22 +92,27 @@ def test_long_split_kv_t131072_np256():
     assert_bf16_close(bf16_bits(outb), oracle.round_bf16(ref))
 
 
-def test_host_tiled_t65536():
+@pytest.mark.parametrize("tiles_per_copy", [1, 8])
+def test_host_tiled_t65536(tiles_per_copy):
+    """The host-tiled workload: 128 tiles of 512 positions, copied one tile
+    per copy (the pages' pipeline) or eight per copy, as the benchmark runs
+    them."""
     w = inputs.WORKLOADS["host_tiled_t64k"]
     q, k, v = inputs.host_tiled_kv()
     dev = "cuda"
     B, Hq, Hkv, tile = w["B"], w["Hq"], w["Hkv"], w["tile"]
     hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-    slots_k = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    slots_v = [torch.empty((B, tile, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    span = tile * tiles_per_copy
+    slots_k = [torch.empty((B, span, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    slots_v = [torch.empty((B, span, Hkv, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     events = [torch.cuda.Event() for _ in range(4)]
     m = torch.empty((B, Hq), device=dev)
     l = torch.empty((B, Hq), device=dev)
     acc = torch.empty((B, Hq, 128), device=dev)
     out = torch.empty((B, Hq, 128), device=dev)
     pg.attn_host_tiled_run(to_device_bf16(q, dev), hk, hv, SCALE, slots_k, slots_v, events, m, l, acc,
-                           out_f32=out, tile_len=tile, copy_stream=torch.cuda.Stream())
+                           out_f32=out, tile_len=tile, tiles_per_copy=tiles_per_copy, copy_stream=torch.cuda.Stream())
     torch.cuda.synchronize()
     ref = oracle.attention_contiguous(q, k, v, SCALE)
     assert np.abs(out.cpu().numpy() - ref).max() <= ATOL_F32

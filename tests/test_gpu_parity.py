@@ -378,14 +378,15 @@ def test_tile_state_resumes_like_a_checkpoint():
         assert np.abs(out.cpu().numpy() - ref).max() <= ATOL_F32
 
 
-def host_tiled(q, k, v, tile=512, n_slots=2):
+def host_tiled(q, k, v, tile=512, n_slots=2, tiles_per_copy=1):
     dev = "cuda"
     B, Hq, D = q.shape
     _, T, Hkv, _ = k.shape
     hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
-    slots_k = [torch.empty((B, tile, Hkv, D), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
-    slots_v = [torch.empty((B, tile, Hkv, D), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
+    span = tile * tiles_per_copy
+    slots_k = [torch.full((B, span, Hkv, D), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
+    slots_v = [torch.full((B, span, Hkv, D), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(n_slots)]
     events = [torch.cuda.Event() for _ in range(2 * n_slots)]
     m = torch.empty((B, Hq), device=dev)
     l = torch.empty((B, Hq), device=dev)
@@ -394,16 +395,21 @@ def host_tiled(q, k, v, tile=512, n_slots=2):
     outb = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
     copy_stream = torch.cuda.Stream()
     pg.attn_host_tiled_run(to_device_bf16(q, dev), hk, hv, SCALE, slots_k, slots_v, events, m, l, acc,
-                           out_f32=out, out_bf16=outb, tile_len=tile, copy_stream=copy_stream)
+                           out_f32=out, out_bf16=outb, tile_len=tile, tiles_per_copy=tiles_per_copy,
+                           copy_stream=copy_stream)
     torch.cuda.synchronize()
     return out.cpu().numpy(), bf16_bits(outb)
 
 
-@pytest.mark.parametrize("B,T,tile,n_slots", [(1, 4096, 512, 2), (2, 1500, 512, 3), (1, 700, 128, 2), (3, 1, 512, 2)])
-def test_host_tiled_run_matches_oracle(B, T, tile, n_slots):
+@pytest.mark.parametrize("B,T,tile,n_slots,per_copy", [
+    (1, 4096, 512, 2, 1), (2, 1500, 512, 3, 1), (1, 700, 128, 2, 1), (3, 1, 512, 2, 1),
+    (1, 4096, 512, 2, 4), (2, 5000, 512, 2, 3), (3, 1300, 128, 3, 2), (1, 100, 512, 2, 8)])
+def test_host_tiled_run_matches_oracle(B, T, tile, n_slots, per_copy):
+    """Copies of one tile (the pages' pipeline) or of several tiles per slot
+    (per_copy), ragged last groups and tiles, several sequences."""
     k, v = inputs.contiguous_kv(96 + T, B, T, 8)
     q = inputs.query(96 + T, B, 16)
-    out, outb = host_tiled(q, k, v, tile, n_slots)
+    out, outb = host_tiled(q, k, v, tile, n_slots, per_copy)
     ref = oracle.attention_contiguous(q, k, v, SCALE)
     assert np.abs(out - ref).max() <= ATOL_F32
     assert_bf16_close(outb, oracle.round_bf16(ref))

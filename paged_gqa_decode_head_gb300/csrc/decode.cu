@@ -62,9 +62,10 @@ constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-by
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
-// Chunks per warp requested before the grid wait (measured on the 28-layer
-// T = 8192 chain): the fused step does best with 1, attention alone with all.
-template <bool kFused> constexpr int kPrewaitChunks = kFused ? 1 : kStages;
+// Chunks per warp requested before the grid wait, measured on the 28-layer
+// T = 8192 chain (NP = 15): the fused step does best with 2 (1: +0.7 us per
+// layer, 3: +0.25 us), attention alone with all.
+template <bool kFused> constexpr int kPrewaitChunks = kFused ? 2 : kStages;
 // Shared memory (from a 1024-byte aligned base): the stages, one mbarrier and
 // one valid-row count per stage, the partition ticket, the merge's mbarrier,
 // the rotated query of the fused step.

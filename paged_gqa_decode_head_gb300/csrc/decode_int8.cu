@@ -527,8 +527,11 @@ __global__ void __launch_bounds__(Shape8<kW>::kWarps * 32, 1)
 
     bool ok = true;
     int k0 = 0;
+    // As in the bf16 kernel: pairs for warps with few chunks, whole groups
+    // otherwise (the grouping depends only on the chunk count).
+    const int group = my_chunks <= 2 * S::kGroup ? 2 : S::kGroup;
     for (int nc; k0 < my_chunks; k0 += nc) {
-        nc = min(S::kGroup, my_chunks - k0);
+        nc = min(group, my_chunks - k0);
         uint32_t stage_addr[S::kGroup];
         const float *scl[S::kGroup];
         int rows[S::kGroup];

@@ -951,15 +951,15 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
         }
         // A layer that fits one wave with each partition inside one CTA's
         // ring (the T = 8192 layer chain) is bound by its chain of latencies,
-        // not by bandwidth: there, leave a fifth of the SMs free for the CTAs
+        // not by bandwidth: there, leave a tenth of the SMs free for the CTAs
         // that merge (which hold their SM while the next layer starts) and
-        // merge fewer partitions. B = 1, T = 8192 on GB300: NP = 15 instead of
-        // 19 is 2 % faster for the bf16 fused step, 1.6 % for attention alone
-        // and 7 % for the INT8 fused step; at T = 32768 and 131072, or B = 2,
+        // merge fewer partitions. B = 1, T = 8192 on GB300: NP = 17 instead of
+        // 19 is 16 % faster for the bf16 fused step, 8 % for attention alone
+        // and 15 % for the INT8 fused step; at T = 32768 and 131072, or B = 2,
         // a full wave stays best.
         const long best_ppp = (max_pages + best - 1) / best;
         if (units * best <= slots && best_ppp * page_size <= kWarps * kStages * kChunkTokens)
-            best = std::min(best, std::max<long>(1, slots * 4 / 5 / units));
+            best = std::min(best, std::max<long>(1, slots * 9 / 10 / units));
         np = best;
     }
     np = std::min<long>(std::max<long>(np, 1), std::min(max_pages, kMaxPartitions));

@@ -448,12 +448,12 @@ def test_step_chain_prologue_then_attention_and_graph_replay():
 def test_partition_count_follows_the_regime():
     """Automatic partition counts on this GPU: a T = 8192 layer of one
     sequence (latency-bound, every partition inside one CTA's ring) leaves at
-    least a fifth of the SMs free; T = 131072 fills a wave of SMs; a batch
+    least a tenth of the SMs free; T = 131072 fills a wave of SMs; a batch
     that fills the SMs with its (sequence, KV head) units uses few
     partitions (16 sequences of 8192 positions: one each)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     short = pg.decode_attn_partition_count(1, 8, 16, 512, 0)
-    assert 8 * short <= sms * 4 // 5 and short >= 2
+    assert 8 * short <= sms * 9 // 10 and short >= 2
     long_ = pg.decode_attn_partition_count(1, 8, 16, 8192, 0)
-    assert sms * 4 // 5 < 8 * long_ <= sms
+    assert sms * 9 // 10 < 8 * long_ <= sms
     assert pg.decode_attn_partition_count(16, 8, 16, 512, 0) == 1

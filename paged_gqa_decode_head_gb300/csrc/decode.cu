@@ -28,7 +28,9 @@
 //   before griddepcontrol.wait, so one layer's history streams in while the
 //   previous kernels in the stream (the previous layer, this layer's prologue)
 //   finish; the query and the chunk holding the new token are read after it.
-//   With 27 chunks per SM a whole 8192-position, 8-head layer fits.
+//   With 27 chunks per SM a whole 8192-position, 8-head layer nearly fits;
+//   such a latency-bound layer runs on nine tenths of the SMs (the rest take
+//   the previous layer's merging CTAs) and its warps fold in pairs.
 // * The warps' states are merged in shared memory; NP = 1 writes the output,
 //   NP > 1 writes the partition state. With at most kFusedMergeMax
 //   partitions the last CTA of each (sequence, KV head) to finish (a ticket

@@ -65,6 +65,26 @@ def dist_env():
     return rank, world, local
 
 
+def slowest_rank_ms(ms: float, world: int, device) -> float:
+    """The job's time for a timed region: the largest over the ranks (each
+    rank times its own replica; collectives only here, never on the data
+    path)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: float, world: int, step_s: float) -> float:
+    """Whole-job throughput: every rank's bytes of a step over the slowest
+    rank's step time (replicas: per-rank work is fixed, weak scaling)."""
+    return world * bytes_per_rank_step / step_s / 1e9
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -299,14 +319,7 @@ def run_ours(args, rank, world, local):
             fn()
         e1.record(stream)
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return slowest_rank_ms(e0.elapsed_time(e1), world, dev)
 
     for _ in range(max(3, args.warmup)):
         step_graph.replay()
@@ -351,7 +364,7 @@ def run_ours(args, rank, world, local):
     assert pg.device_error_flags() == 0, "device error flags raised during the benchmark"
 
     step_s = ms / args.steps / 1e3
-    value = world * kv_bytes / step_s / 1e9
+    value = job_gbs(kv_bytes, world, step_s)
     layer_attn_s = ms_attn / args.steps / 1e3 / n_layers
     achieved = algo_bytes_step / (step_s / n_layers) / 1e9
     achieved_attn = algo_bytes_attn / layer_attn_s / 1e9
@@ -380,7 +393,7 @@ def run_ours(args, rank, world, local):
                      "attention_only": {"achieved": achieved_attn, "frac": achieved_attn / peak,
                                         "bytes_per_launch": algo_bytes_attn,
                                         "kernel": "decode_mma_kernel<2> (decode_attn_paged), attention-only graph"}},
-        "e2e": {"value": world * kv_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_gbs(kv_bytes, world, e2e_s), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * n_layers * launches_per_layer,
         "clocks": clocks,

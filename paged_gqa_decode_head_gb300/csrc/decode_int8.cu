@@ -11,11 +11,12 @@
 // Cache: codes int8 [num_pages][Hkv][P][128] (symmetric, per row), scales
 // float [num_pages][Hkv][P] for K and for V.
 //
-// GB300 design, as the bf16 kernel: one 288-thread CTA per SM, 9 warps each
-// owning every 9th 16-position chunk and a ring of 3 stages; a chunk is two
-// 2 KiB TMA tiles (K, V: 16 rows x 128 bytes, 128-byte swizzle) plus the
-// chunk's 2 x 64 bytes of scales by bulk copy, all completing on one
-// mbarrier. The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
+// GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
+// kW-th 16-position chunk of the partition and a private ring of stages (9
+// warps x 6 stages for short partitions, 12 warps x 4 for long ones: see
+// Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
+// 128-byte swizzle) plus the chunk's 2 x 64 bytes of scales by bulk copy, all
+// completing on one mbarrier. The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
 // converted in registers: ldmatrix hands a lane four consecutive bytes of a
 // row, so the MMA's k index (S^T = K Q^T) and M index (O^T = V^T P^T) are
 // taken in a fixed permutation of the 16 dims of a step -- the query is loaded

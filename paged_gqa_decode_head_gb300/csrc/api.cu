@@ -266,6 +266,7 @@ static int attn_impl(const char *fn, int M, const pgqa_bf16 *q, const pgqa_bf16 
     a.out_bf16 = out_bf16;
     a.ws = static_cast<float *>(workspace);
     a.M = M;
+    a.sm_count = sm_count_current_device();
     cudaError_t err = pgqa::launch_decode(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);
@@ -365,6 +366,7 @@ static int step_impl(const char *fn, int M, const pgqa_bf16 *q, const pgqa_bf16 
     a.ws = static_cast<float *>(workspace);
     a.fused = true;
     a.M = M;
+    a.sm_count = sm_count_current_device();
     a.q_raw = q;
     a.k_new = k;
     a.v_new = v;

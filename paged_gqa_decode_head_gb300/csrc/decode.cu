@@ -14,9 +14,12 @@
 // GB300 design.
 // * Grid = (partition, KV head, sequence), one 288-thread CTA per SM. Each of
 //   the 9 warps owns every 9th 16-position chunk of the partition and a
-//   private ring of 3 shared-memory stages (27 chunks = 216 KiB per CTA). Lane
-//   0 issues one 3-D TMA load per 4 KiB chunk of K and of V (16 rows, two
-//   64-column halves, 128-byte swizzle) that complete on the stage's mbarrier.
+//   private ring of 3 shared-memory stages (27 chunks = 216 KiB per CTA).
+//   Grids of several waves with short partitions (a forced partition count)
+//   run two CTAs per SM instead, 6 warps x 2 stages each, so that one CTA's
+//   start and end overlap the other's streaming. Lane 0 of a warp issues
+//   one 3-D TMA load per 4 KiB chunk of K and of V (16 rows, two 64-column
+//   halves, 128-byte swizzle) that complete on the stage's mbarrier.
 // * The warp folds its resident chunks together with tensor-core MMAs
 //   (mma.sync m16n8k16, bf16 in, fp32 accumulate), transposed so the g <= 8
 //   query heads fill the N = 8 columns: S^T = K Q^T, the online softmax on the
@@ -56,33 +59,53 @@ __device__ unsigned g_flags_decode;
 
 __device__ __forceinline__ void raise_flag(unsigned f) { atomicOr(&g_flags_decode, f); }
 
-// One CTA per SM holding 27 staged chunks (216 KiB): across 152 SMs that is
-// more than a whole 8192-position layer of one 8-head KV cache.
-constexpr int kWarps = 9;
-constexpr int kStages = 3;
 constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
-constexpr int kCtasPerSm = 1;                   // what the shared-memory footprint allows
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
+
+// CTA shape: kW warps, each with a ring of kS chunk stages, kCtas CTAs per
+// SM. Shared memory (from a 1024-byte aligned base): the stages, one
+// mbarrier and one valid-row count per stage, the partition ticket, the
+// merge's mbarrier, the rotated query and the new K, V rows of the fused step.
+template <int kW, int kS, int kCtas> struct Shape {
+    static constexpr int kWarps = kW;
+    static constexpr int kStages = kS;
+    static constexpr int kCtasPerSm = kCtas;
+    static constexpr int kThreads = kW * 32;
+    static constexpr int kStageAreaBytes = kW * kS * kStageBytes;
+    static constexpr int kBarOffset = kStageAreaBytes;
+    static constexpr int kRowsOffset = kBarOffset + kW * kS * 8;
+    static constexpr int kTicketOffset = (kRowsOffset + kW * kS * 4 + 7) & ~7;
+    static constexpr int kMergeBarOffset = kTicketOffset + 8;
+    static constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
+    static constexpr int kPatchOffset = kQBufOffset + kMaxGroup * kHeadDim * 2;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kPatchOffset + 4 * kHeadDim;
+    // The in-kernel merge copies the G x n partition accumulators of its
+    // group into the stage area, followed by its scratch (weights, sums, a
+    // float4 per thread); launch_decode falls back to merge_kernel when they
+    // do not fit.
+    static constexpr int kMergeScratchBytes = merge_scratch_bytes<kThreads, kFusedMergeMax>(kMaxGroup);
+    static_assert(kSmem <= 232448, "at most 227 KB of shared memory per CTA");
+    static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
+};
+// One CTA per SM holding 27 staged chunks (216 KiB): across 152 SMs that is
+// more than a whole 8192-position layer of one 8-head KV cache. Used for
+// every grid that fits one wave and for long partitions.
+using SoloShape = Shape<9, 3, 1>;
+// Two CTAs per SM of 6 warps x 2 stages (96 KiB each): for grids of several
+// waves with short partitions, where one CTA's start (table and context
+// loads, first request) and end (merge, state write) overlap the other's
+// streaming. B = 1, Hq = 32, T = 131072 with 512-position partitions (2048
+// CTAs): 96.8 vs 113.3 us; 2048-position partitions 87.8 vs 95.0 us.
+using PairShape = Shape<6, 2, 2>;
+// Longest partition (positions) the two-CTA shape takes: B = 64 ragged
+// contexts with 4096-position partitions run 1 % faster on SoloShape.
+constexpr int kPairMaxPositions = 2048;
+
 // Chunks per warp requested before the grid wait, measured on the 28-layer
 // T = 8192 chain (NP = 15): the fused step does best with 2 (1: +0.7 us per
 // layer, 3: +0.25 us), attention alone with all.
-template <bool kFused> constexpr int kPrewaitChunks = kFused ? 2 : kStages;
-// Shared memory (from a 1024-byte aligned base): the stages, one mbarrier and
-// one valid-row count per stage, the partition ticket, the merge's mbarrier,
-// the rotated query of the fused step.
-constexpr int kStageAreaBytes = kWarps * kStages * kStageBytes;
-constexpr int kBarOffset = kStageAreaBytes;
-constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
-constexpr int kTicketOffset = (kRowsOffset + kWarps * kStages * 4 + 7) & ~7;
-constexpr int kMergeBarOffset = kTicketOffset + 8;
-constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
-constexpr int kPatchOffset = kQBufOffset + kMaxGroup * kHeadDim * 2; // fused step: new K, V rows (bf16)
-constexpr int kSplitSmem = 1024 /* alignment slack */ + kPatchOffset + 4 * kHeadDim;
-// The in-kernel merge copies the G x n partition accumulators of its group
-// into the stage area, followed by its scratch (weights, sums, a float4 per
-// thread); launch_decode falls back to merge_kernel when they do not fit.
-constexpr int kMergeScratchBytes = merge_scratch_bytes<kWarps * 32, kFusedMergeMax>(kMaxGroup);
+template <bool kFused, int kStages> constexpr int kPrewaitChunks = kFused && kStages > 2 ? 2 : kStages;
 
 struct SplitParams {
     const uint16_t *q;
@@ -156,10 +179,11 @@ template <int NCOL> struct MmaWarp {
     // stage[c] is the shared address of chunk c's four swizzled boxes; keys
     // from row lim0[c] (lim1[c]) on are masked out for column 2t (2t+1) --
     // the chunk's valid rows, cut further by a column's causal limit.
-    template <int NC, bool kPerColumn>
-    __device__ __forceinline__ void fold(const uint32_t (&stage)[kStages], const int (&lim0)[kStages],
-                                         const int (&lim1)[kStages], float scale_log2)
+    template <int NC, bool kPerColumn, int N>
+    __device__ __forceinline__ void fold(const uint32_t (&stage)[N], const int (&lim0)[N], const int (&lim1)[N],
+                                         float scale_log2)
     {
+        static_assert(NC <= N, "one stage per folded chunk");
         const int lane = threadIdx.x & 31, g = lane >> 2;
         const int mq = lane >> 3, mr = lane & 7; // ldmatrix: matrix index, row within it
 
@@ -309,12 +333,12 @@ template <int NCOL> struct MmaWarp {
 
 // The last CTA of a (sequence, KV head) to finish merges the n (2..64)
 // partition states of its columns (partition_merge.cuh).
-template <int NCOL, bool kMulti>
+template <int NCOL, bool kMulti, int kThreads>
 __device__ __forceinline__ void merge_in_last_cta(const SplitParams &p, int b, int kvh, int n,
                                                   unsigned char *smem, uint64_t *bar)
 {
     const auto row_of = [&](int c) { return column_row<kMulti>(p, b, kvh, c); };
-    if (!merge_partitions_in_cta<NCOL, kWarps * 32, kFusedMergeMax>(p.ws_m, p.ws_l, p.ws_acc, p.NP, n, row_of,
+    if (!merge_partitions_in_cta<NCOL, kThreads, kFusedMergeMax>(p.ws_m, p.ws_l, p.ws_acc, p.NP, n, row_of,
                                                                      p.out_f32, p.out_bf16, smem, bar) &&
         threadIdx.x == 0)
         raise_flag(PGQA_DEVERR_WAIT_TIMEOUT); // the merge's copy never landed: outputs left alone
@@ -327,11 +351,16 @@ __device__ __forceinline__ void merge_in_last_cta(const SplitParams &p, int b, i
 // chunk, so every history chunk can be requested before griddepcontrol.wait.
 // NCOL = M * G columns; kMulti: M > 1 new tokens (not fused), each column
 // with its own causal limit.
-template <int NCOL, bool kFused, bool kMulti>
-__global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
+template <int NCOL, bool kFused, bool kMulti, typename S>
+__global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const SplitParams p)
 {
+    constexpr int kWarps = S::kWarps, kStages = S::kStages;
+    constexpr int kBarOffset = S::kBarOffset, kRowsOffset = S::kRowsOffset, kTicketOffset = S::kTicketOffset;
+    constexpr int kMergeBarOffset = S::kMergeBarOffset, kQBufOffset = S::kQBufOffset;
+    constexpr int kPatchOffset = S::kPatchOffset;
+    constexpr int kPrewait = kPrewaitChunks<kFused, kStages>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -428,14 +457,14 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
-    // Only the first kPrewaitChunks chunks of each warp are requested before
+    // Only the first kPrewait chunks of each warp are requested before
     // griddepcontrol.wait: in the fused step the rest would queue in the
     // memory system ahead of the previous layer's merge and this layer's
     // query loads, which sit on the critical path of the layer chain.
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && k < kPrewaitChunks<kFused> && !holds_new_token(k))
+            if (k < first && k < kPrewait && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
 
@@ -509,7 +538,7 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k)
-            if (k < first && (k >= kPrewaitChunks<kFused> || holds_new_token(k)) &&
+            if (k < first && (k >= kPrewait || holds_new_token(k)) &&
                 !(kDeferNew && holds_new_token(k)))
                 issue(k, first_phys[k], policy);
     }
@@ -657,12 +686,19 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
         }
         if (!ok)
             break;
-        if (nc == 3)
-            st.template fold<3, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
-        else if (nc == 2)
-            st.template fold<2, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
-        else
-            st.template fold<1, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+        if constexpr (kStages >= 3) {
+            if (nc == 3)
+                st.template fold<3, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+            else if (nc == 2)
+                st.template fold<2, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+            else
+                st.template fold<1, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+        } else {
+            if (nc == 2)
+                st.template fold<2, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+            else
+                st.template fold<1, kMulti>(stage_addr, lim0, lim1, p.scale_log2);
+        }
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < kStages; ++c) {
@@ -741,7 +777,8 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm)
     __syncthreads();
     if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
         return;
-    merge_in_last_cta<NCOL, kMulti>(p, b, kvh, n_parts, smem, reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
+    merge_in_last_cta<NCOL, kMulti, S::kThreads>(p, b, kvh, n_parts, smem,
+                                                 reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
     if (threadIdx.x == 0)
         *ticket = 0u; // ready for the next call
 }
@@ -874,7 +911,7 @@ cudaError_t encode_cache_map(CUtensorMap *map, const void *base, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NCOL, bool kFused, bool kMulti>
+template <int NCOL, bool kFused, bool kMulti, typename S>
 cudaError_t launch_split_t(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
                            dim3 grid, cudaStream_t stream)
 {
@@ -884,26 +921,41 @@ cudaError_t launch_split_t(const CUtensorMap &mk, const CUtensorMap &mv, const S
     if (err != cudaSuccess)
         return err;
     if (dev >= kMaxDevices || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_mma_kernel<NCOL, kFused, kMulti>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmem);
+        err = cudaFuncSetAttribute(decode_mma_kernel<NCOL, kFused, kMulti, S>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < kMaxDevices)
             configured[dev] = true;
     }
-    return launch_pdl(decode_mma_kernel<NCOL, kFused, kMulti>, grid, dim3(kWarps * 32), kSplitSmem, stream, mk,
-                      mv, kp);
+    return launch_pdl(decode_mma_kernel<NCOL, kFused, kMulti, S>, grid, dim3(S::kThreads), S::kSmem, stream,
+                      mk, mv, kp);
 }
 
+// pair: the two-CTA shape (single token, NCOL <= its warps; the caller checks).
 template <int NCOL>
 cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp,
-                         dim3 grid, bool fused, cudaStream_t stream)
+                         dim3 grid, bool fused, bool pair, cudaStream_t stream)
 {
     if (kp.M > 1)
-        return fused ? launch_split_t<NCOL, true, true>(mk, mv, kp, grid, stream)
-                     : launch_split_t<NCOL, false, true>(mk, mv, kp, grid, stream);
-    return fused ? launch_split_t<NCOL, true, false>(mk, mv, kp, grid, stream)
-                 : launch_split_t<NCOL, false, false>(mk, mv, kp, grid, stream);
+        return fused ? launch_split_t<NCOL, true, true, SoloShape>(mk, mv, kp, grid, stream)
+                     : launch_split_t<NCOL, false, true, SoloShape>(mk, mv, kp, grid, stream);
+    if constexpr (NCOL <= PairShape::kWarps) {
+        if (pair)
+            return fused ? launch_split_t<NCOL, true, false, PairShape>(mk, mv, kp, grid, stream)
+                         : launch_split_t<NCOL, false, false, PairShape>(mk, mv, kp, grid, stream);
+    }
+    return fused ? launch_split_t<NCOL, true, false, SoloShape>(mk, mv, kp, grid, stream)
+                 : launch_split_t<NCOL, false, false, SoloShape>(mk, mv, kp, grid, stream);
+}
+
+// The two-CTA shape takes single-token grids of more than one wave (of one
+// CTA per SM) whose partitions are short; the fused step and attention alone
+// follow the same rule, so they keep giving equal bits.
+bool use_pair_shape(int NCOL, int M, int B, int Hkv, int num_partitions, int part_positions, int sm_count)
+{
+    return M == 1 && NCOL <= PairShape::kWarps && num_partitions > 1 && part_positions <= kPairMaxPositions &&
+           static_cast<long>(B) * Hkv * num_partitions > static_cast<long>(sm_count > 0 ? sm_count : 1);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -933,7 +985,7 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
         // to 12 (NP = 2: 4 % slower).
         constexpr long kCtaCostPositions = 600;
         const long units = static_cast<long>(B) * Hkv;
-        const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * kCtasPerSm;
+        const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * SoloShape::kCtasPerSm;
         const long lo = std::max(1, 128 / page_size);
         const long max_np = std::max<long>(1, std::min<long>((max_pages + lo - 1) / lo, 2 * slots));
         const long hi_pages = std::max(1, 4096 / page_size);
@@ -960,7 +1012,8 @@ int choose_partitions(int B, int Hkv, int page_size, int max_pages, int requeste
         // and 15 % for the INT8 fused step; at T = 32768 and 131072, or B = 2,
         // a full wave stays best.
         const long best_ppp = (max_pages + best - 1) / best;
-        if (units * best <= slots && best_ppp * page_size <= kWarps * kStages * kChunkTokens)
+        if (units * best <= slots &&
+            best_ppp * page_size <= SoloShape::kWarps * SoloShape::kStages * kChunkTokens)
             best = std::min(best, std::max<long>(1, slots * 9 / 10 / units));
         np = best;
     }
@@ -1030,11 +1083,15 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
-    kp.fused_merge = a.num_partitions <= kFusedMergeMax &&
-                             static_cast<long>(NCOL) * a.num_partitions * kHeadDim * 4 + kMergeScratchBytes <=
-                                 kStageAreaBytes
-                         ? 1
-                         : 0;
+    const bool pair = use_pair_shape(NCOL, M, a.B, a.Hkv, a.num_partitions, a.pages_per_part * a.page_size,
+                                     a.sm_count);
+    const long merge_bytes = static_cast<long>(NCOL) * a.num_partitions * kHeadDim * 4 +
+                             (pair ? PairShape::kMergeScratchBytes : SoloShape::kMergeScratchBytes);
+    kp.fused_merge =
+        a.num_partitions <= kFusedMergeMax &&
+                merge_bytes <= (pair ? PairShape::kStageAreaBytes : SoloShape::kStageAreaBytes)
+            ? 1
+            : 0;
     if (a.fused) {
         kp.q_raw = a.q_raw;
         kp.k_new = a.k_new;
@@ -1060,14 +1117,14 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.G = G;
     kp.M = M;
     switch (NCOL) {
-    case 1: err = launch_split<1>(mk, mv, kp, grid, a.fused, stream); break;
-    case 2: err = launch_split<2>(mk, mv, kp, grid, a.fused, stream); break;
-    case 3: err = launch_split<3>(mk, mv, kp, grid, a.fused, stream); break;
-    case 4: err = launch_split<4>(mk, mv, kp, grid, a.fused, stream); break;
-    case 5: err = launch_split<5>(mk, mv, kp, grid, a.fused, stream); break;
-    case 6: err = launch_split<6>(mk, mv, kp, grid, a.fused, stream); break;
-    case 7: err = launch_split<7>(mk, mv, kp, grid, a.fused, stream); break;
-    case 8: err = launch_split<8>(mk, mv, kp, grid, a.fused, stream); break;
+    case 1: err = launch_split<1>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 2: err = launch_split<2>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 3: err = launch_split<3>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 4: err = launch_split<4>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 5: err = launch_split<5>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 6: err = launch_split<6>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 7: err = launch_split<7>(mk, mv, kp, grid, a.fused, pair, stream); break;
+    case 8: err = launch_split<8>(mk, mv, kp, grid, a.fused, pair, stream); break;
     default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)

@@ -36,6 +36,7 @@ struct DecodeArgs {
     pgqa_bf16 *out_bf16; // nullable
     float *ws;           // partial states when NP > 1
     int M; // new tokens (queries) per sequence; 0 or 1 = the single-token step
+    int sm_count; // SMs of the device (selects the CTA shape)
     // fused decode step (qk_norm_rope_append + attention in one launch)
     bool fused;
     const pgqa_bf16 *q_raw, *k_new, *v_new, *gamma_q, *gamma_k;

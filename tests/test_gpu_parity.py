@@ -199,6 +199,42 @@ def test_decode_many_partitions_use_the_merge_kernel(num_partitions):
     check_attention(q, kv, num_partitions)
 
 
+def two_cta_shape(B, Hq, Hkv, P, max_pages, num_partitions):
+    """The library's rule for its two-CTAs-per-SM kernel shape (6 warps x 2
+    stages): one new token, g <= 6, more CTAs than SMs and partitions of at
+    most 2048 positions."""
+    np_used = pg.decode_attn_partition_count(B, Hkv, P, max_pages, num_partitions)
+    ppp = -(-max_pages // np_used)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return Hq // Hkv <= 6 and np_used > 1 and ppp * P <= 2048 and B * Hkv * np_used > sms
+
+
+@pytest.mark.parametrize("Hq,num_partitions", [(8, 64), (16, 32), (32, 24), (48, 40), (48, 8)])
+def test_decode_two_cta_shape_in_kernel_and_kernel_merges(Hq, num_partitions):
+    # several waves of short partitions run the two-CTA shape; (48, 40) has
+    # more accumulators than its stage area holds and merges in merge_kernel,
+    # the others in the last CTA; empty and one-position sequences included
+    ctx = [2048, 1, 0, 1500, 2047, 700, 2048, 33]
+    kv = inputs.paged_kv(95 + Hq, ctx, Hkv=8, page_size=16)
+    q = inputs.query(95 + Hq, len(ctx), Hq)
+    assert two_cta_shape(len(ctx), Hq, 8, 16, kv.max_pages, num_partitions)
+    check_attention(q, kv, num_partitions)
+
+
+def test_decode_two_cta_shape_is_taken_only_for_short_partitions_in_several_waves():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # the T = 8192 layer chain and a long single sequence fit one wave
+    assert not two_cta_shape(1, 16, 8, 16, 512, 0)
+    assert not two_cta_shape(1, 32, 8, 16, 8192, 0)
+    # 512-position partitions of T = 131072: 2048 CTAs
+    assert two_cta_shape(1, 32, 8, 16, 8192, 256)
+    # 4096-position partitions stay on the one-CTA shape
+    assert not two_cta_shape(1, 32, 8, 16, 8192, 32)
+    # groups of 8 query heads need the one-CTA shape's 9 warps
+    assert not two_cta_shape(1, 64, 8, 16, 8192, 256)
+    assert 8 * 256 > sms
+
+
 def test_decode_repeated_calls_reuse_the_workspace():
     # the partition tickets must come back to zero after every call
     kv = inputs.paged_kv(87, [2000, 3001], Hkv=8, page_size=16)

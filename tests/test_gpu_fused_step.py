@@ -130,6 +130,25 @@ def test_fused_step_matches_the_two_launches_bit_for_bit(num_partitions):
     assert np.array_equal(fused["of"], two["of"])
 
 
+@pytest.mark.parametrize("Hq", [8, 24, 48])
+def test_fused_step_two_cta_shape(Hq):
+    # several waves of short partitions (8 sequences x 8 KV heads x 40
+    # partitions of 64 positions) run the two-CTA shape, 6 warps: g = 1, 3
+    # and 6 (as many query heads per KV head as it has warps to rotate them);
+    # against the oracle and bit for bit against the two launches
+    ctx = [2048, 1, 2, 1500, 2047, 700, 2048, 33]
+    kv = inputs.paged_kv(380 + Hq, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    tok = inputs.new_token(380 + Hq, len(ctx), Hq, 8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    np_used = pg.decode_attn_partition_count(len(ctx), 8, 16, kv.max_pages, 40)
+    assert np_used > 1 and len(ctx) * 8 * np_used > sms and -(-kv.max_pages // np_used) * 16 <= 2048
+    fused = check_fused(kv, tok, 40)
+    two = run_unfused(kv, tok, 40)
+    for key in ("q_out", "kc", "vc", "ob"):
+        assert np.array_equal(fused[key], two[key]), key
+    assert np.array_equal(fused["of"], two["of"])
+
+
 def test_fused_step_flags_empty_context_and_bad_page():
     kv = inputs.paged_kv(370, [40, 40], Hkv=8, page_size=16, fill_unused="normal")
     tok = inputs.new_token(370, 2, 16, 8)

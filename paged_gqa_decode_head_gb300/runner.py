@@ -134,16 +134,40 @@ class DecodeStep:
         for i in range(len(self.layers)):
             self.run_layer(i, stream=stream, prologue=prologue, fused=fused)
 
-    def capture(self, prologue: bool = True, fused: bool = False) -> torch.cuda.CUDAGraph:
-        """Record one whole step (every layer) into a CUDA graph."""
+    def capture(self, prologue: bool = True, fused: bool = False, host_in: torch.Tensor | None = None,
+                host_out: torch.Tensor | None = None) -> torch.cuda.CUDAGraph:
+        """Record one whole step (every layer) into a CUDA graph.
+
+        With ``host_in`` (pinned, bf16, shaped like ``new_tokens``) the graph
+        starts with the copy of the step's new tokens from it; with
+        ``host_out`` (pinned, fp32, shaped like ``outputs``) it ends with the
+        copy of every layer's output into it. A replay is then one whole step
+        from host inputs to host results; synchronise before reading
+        ``host_out``."""
+        if host_in is not None and (host_in.device.type != "cpu" or not host_in.is_pinned()
+                                    or host_in.dtype != torch.bfloat16
+                                    or host_in.numel() != self.new_tokens.numel()):
+            raise ValueError("host_in must be pinned host bf16 memory with new_tokens' element count")
+        if host_out is not None and (host_out.device.type != "cpu" or not host_out.is_pinned()
+                                     or host_out.dtype != torch.float32
+                                     or host_out.shape != self.outputs.shape):
+            raise ValueError("host_out must be pinned host fp32 memory shaped like outputs")
+
+        def step():
+            if host_in is not None:
+                self.new_tokens.copy_(host_in.view(-1), non_blocking=True)
+            self.run(prologue=prologue, fused=fused)
+            if host_out is not None:
+                host_out.copy_(self.outputs, non_blocking=True)
+
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
-            self.run(prologue=prologue, fused=fused)  # warm-up outside capture
+            step()  # warm-up outside capture
         torch.cuda.current_stream(self.device).wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(prologue=prologue, fused=fused)
+            step()
         self.graph = g
         return g
 

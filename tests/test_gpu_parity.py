@@ -481,6 +481,35 @@ def test_step_chain_prologue_then_attention_and_graph_replay():
     assert pg.device_error_flags() == 0
 
 
+def test_step_graph_with_host_io():
+    """A step graph that starts with the copy of the new tokens from pinned
+    host memory and ends with the copy of the outputs back: its host results
+    equal the outputs of the same step run eagerly from device inputs."""
+    layers = []
+    for i in range(2):
+        kv = inputs.paged_kv(110 + i, [300, 17], Hkv=8, page_size=16, fill_unused="normal")
+        layers.append((kv, inputs.new_token(110 + i, 2, 16, 8)))
+    eager = DecodeStep(layers, Hq=16, Hkv=8, rope_theta=THETA)
+    eager.run(fused=True)
+    torch.cuda.synchronize()
+    step = DecodeStep(layers, Hq=16, Hkv=8, rope_theta=THETA)
+    host_in = step.new_tokens.cpu().pin_memory()
+    host_out = torch.full(step.outputs.shape, float("nan"), dtype=torch.float32).pin_memory()
+    step.new_tokens.zero_()
+    g = step.capture(fused=True, host_in=host_in, host_out=host_out)
+    # the warm-up run before the capture already appended the new rows; the
+    # replay appends them again (same slots, same values) and recomputes
+    host_out.fill_(float("nan"))
+    step.new_tokens.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(host_out, eager.outputs.cpu())
+    assert torch.equal(step.new_tokens.cpu().view(torch.int16), host_in.view(torch.int16))
+    with pytest.raises(ValueError):
+        step.capture(host_in=host_in.to(torch.float32).pin_memory())
+    assert pg.device_error_flags() == 0
+
+
 def test_partition_count_follows_the_regime():
     """Automatic partition counts on this GPU: a T = 8192 layer of one
     sequence (latency-bound, every partition inside one CTA's ring) leaves at

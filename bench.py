@@ -132,6 +132,27 @@ def smi_gpu_id(dev) -> str:
         return str(idx)
 
 
+def gpu_idle_check(gpu_id: str) -> dict:
+    """Whether the GPU is idle before the benchmark starts: its utilization and
+    the compute processes on it other than this one (nvidia-smi)."""
+    out = {"util_pct": None, "other_processes": None}
+    try:
+        util = subprocess.run(["nvidia-smi", "-i", gpu_id, "--query-gpu=utilization.gpu",
+                               "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+        apps = subprocess.run(["nvidia-smi", "-i", gpu_id, "--query-compute-apps=pid", "--format=csv,noheader"],
+                              capture_output=True, text=True, timeout=20)
+    except (OSError, subprocess.TimeoutExpired):
+        return out
+    try:
+        out["util_pct"] = float(util.stdout.strip().splitlines()[0])
+    except (ValueError, IndexError):
+        pass
+    if apps.returncode == 0:
+        pids = [ln.strip() for ln in apps.stdout.splitlines() if ln.strip().isdigit()]
+        out["other_processes"] = sum(1 for pid in pids if int(pid) != os.getpid())
+    return out
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples in the background (200 ms period)."""
 
@@ -267,6 +288,9 @@ def run_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    # before any work of ours: the GPU should be idle (no other compute
+    # process, no utilization left from an earlier job)
+    idle = gpu_idle_check(smi_gpu_id(dev))
     if world > 1:
         import torch.distributed as dist
 
@@ -398,6 +422,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": args.steps * n_layers * launches_per_layer,
         "clocks": clocks,
+        "gpu_idle_at_start": idle,
         "cpu_baseline": cpu_baseline,
     }
     if rank == 0:

@@ -65,3 +65,34 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 
     bench.run_reference(Args(), 1, 2)
     assert capsys.readouterr().out == ""
+
+
+def _fake_smi(tmp_path, util: str, pids: list[int]) -> str:
+    """A stand-in nvidia-smi answering the two idle-check queries."""
+    script = tmp_path / "nvidia-smi"
+    pid_lines = "\n".join(str(p) for p in pids)
+    script.write_text("#!/bin/sh\n"
+                      "case \"$*\" in\n"
+                      f"  *utilization.gpu*) echo '{util}' ;;\n"
+                      f"  *compute-apps*) printf '%s\\n' '{pid_lines}' ;;\n"
+                      "esac\n")
+    script.chmod(0o755)
+    return str(tmp_path)
+
+
+def test_gpu_idle_check_reads_utilization_and_other_processes(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("PATH", _fake_smi(tmp_path, "37", [os.getpid(), 4242, 4343]) + os.pathsep +
+                       os.environ.get("PATH", ""))
+    got = bench.gpu_idle_check("0")
+    assert got == {"util_pct": 37.0, "other_processes": 2}  # this process is not counted
+
+
+def test_gpu_idle_check_without_nvidia_smi(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    monkeypatch.setenv("PATH", str(tmp_path))  # nothing named nvidia-smi here
+    assert bench.gpu_idle_check("0") == {"util_pct": None, "other_processes": None}

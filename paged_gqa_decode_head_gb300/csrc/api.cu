@@ -803,6 +803,7 @@ static int int8_attn_impl(const char *fn, bool fused, const pgqa_bf16 *q, const 
         a.rope_theta = static_cast<double>(rope_theta);
         a.eps = eps;
     }
+    a.sm_count = sm_count_current_device();
     cudaError_t err = pgqa::launch_decode_int8(a, stream);
     if (err != cudaSuccess)
         return cuda_fail(err, fn);

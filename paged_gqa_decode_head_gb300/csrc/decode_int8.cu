@@ -13,8 +13,9 @@
 //
 // GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
 // kW-th 16-position chunk of the partition and a private ring of stages (9
-// warps x 6 stages for short partitions, 12 warps x 4 for long ones: see
-// Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
+// warps x 6 stages for short partitions, 12 warps x 4 for long ones, and two
+// CTAs per SM of 6 warps x 4 for grids of several waves with short
+// partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
 // 128-byte swizzle) plus the chunk's 2 x 64 bytes of scales by bulk copy, all
 // completing on one mbarrier. The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
 // converted in registers: ldmatrix hands a lane four consecutive bytes of a
@@ -58,14 +59,12 @@ constexpr int kFusedMergeMax8 = 64;                // partitions the last CTA me
 constexpr int kDeepChunks8 = 64;
 
 // CTA shapes: kW warps, each owning every kW-th chunk of its partition in a
-// ring of kStages stages folded kGroup at a time (two groups: one loads while
-// the other folds). 9 warps x 6 stages suit short partitions (the T = 8192
-// layer chain: 3 chunks per warp, all in flight at once); 12 warps x 4 stages
-// spread evenly over the SM's four sub-partitions (9 warps leave one of them
-// with three), which long partitions, bound by the fold, need.
-template <int kW> struct Shape8 {
+// ring of kS stages folded kGroup at a time (two groups: one loads while the
+// other folds), kCtas CTAs per SM.
+template <int kW, int kS, int kCtas> struct Shape8 {
     static constexpr int kWarps = kW;
-    static constexpr int kStages = kW == 12 ? 4 : 6;
+    static constexpr int kStages = kS;
+    static constexpr int kCtasPerSm = kCtas;
     static constexpr int kGroup = kStages / 2; // chunks folded together
     static constexpr int kStageArea = kWarps * kStages * kStage8;
     static constexpr int kScaleOffset = kStageArea;
@@ -85,8 +84,22 @@ template <int kW> struct Shape8 {
     // stages, 9.20 with 4, 9.32 with 3, 9.59 with 2)
     template <bool kFused> static constexpr int kPrewait = kStages;
     static_assert(kSmem <= 232448, "exceeds the 227 KiB of shared memory a CTA may hold");
+    static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
     static_assert(kGroup >= 1 && kGroup <= 3, "fold groups of 1 to 3 chunks");
 };
+// 9 warps x 6 stages suit short partitions in one wave (the T = 8192 layer
+// chain: 3 chunks per warp, all in flight at once).
+using Shape8Short = Shape8<9, 6, 1>;
+// 12 warps x 4 stages spread evenly over the SM's four sub-partitions (9
+// warps leave one of them with three), which long partitions, bound by the
+// fold, need.
+using Shape8Deep = Shape8<12, 4, 1>;
+// Two CTAs per SM of 6 warps x 4 stages (about 100 KiB each) for grids of
+// several waves with short partitions: one CTA's start and end overlap the
+// other's streaming.
+using Shape8Pair = Shape8<6, 4, 2>;
+// Longest partition (positions) the two-CTA shape takes.
+constexpr int kPairMaxPositions8 = 2048;
 
 struct Int8Params {
     const uint16_t *q;
@@ -332,12 +345,11 @@ template <int G> struct Int8Warp {
     }
 };
 
-template <int G, bool kFused, int kW>
-__global__ void __launch_bounds__(Shape8<kW>::kWarps * 32, 1)
+template <int G, bool kFused, typename S>
+__global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const Int8Params p)
 {
-    using S = Shape8<kW>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -676,44 +688,49 @@ cudaError_t encode_int8_map(CUtensorMap *map, const void *base, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int G, bool kFused, int kW>
+template <int G, bool kFused, typename S>
 cudaError_t launch_int8_t(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
                           cudaStream_t stream)
 {
-    using S = Shape8<kW>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
     if (dev >= 64 || !configured[dev]) {
-        err = cudaFuncSetAttribute(decode_int8_kernel<G, kFused, kW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(decode_int8_kernel<G, kFused, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    S::kSmem);
         if (err != cudaSuccess)
             return err;
         if (dev < 64)
             configured[dev] = true;
     }
-    return launch_pdl(decode_int8_kernel<G, kFused, kW>, grid, dim3(S::kWarps * 32), S::kSmem, stream, mk, mv,
+    return launch_pdl(decode_int8_kernel<G, kFused, S>, grid, dim3(S::kWarps * 32), S::kSmem, stream, mk, mv,
                       kp);
 }
 
-template <int kW> bool merges_in_kernel(int G, int num_partitions)
+template <typename S> bool merges_in_kernel(int G, int num_partitions)
 {
-    using S = Shape8<kW>;
     return num_partitions <= kFusedMergeMax8 &&
            static_cast<long>(G) * num_partitions * kHeadDim * 4 + S::kMergeScratch <= S::kStageArea;
 }
 
+enum class Shape8Kind { kShort, kDeep, kPair };
+
 template <int G>
 cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
-                          bool fused, bool deep, cudaStream_t stream)
+                          bool fused, Shape8Kind shape, cudaStream_t stream)
 {
-    if (deep)
-        return fused ? launch_int8_t<G, true, 12>(mk, mv, kp, grid, stream)
-                     : launch_int8_t<G, false, 12>(mk, mv, kp, grid, stream);
-    return fused ? launch_int8_t<G, true, 9>(mk, mv, kp, grid, stream)
-                 : launch_int8_t<G, false, 9>(mk, mv, kp, grid, stream);
+    if constexpr (G <= Shape8Pair::kWarps) {
+        if (shape == Shape8Kind::kPair)
+            return fused ? launch_int8_t<G, true, Shape8Pair>(mk, mv, kp, grid, stream)
+                         : launch_int8_t<G, false, Shape8Pair>(mk, mv, kp, grid, stream);
+    }
+    if (shape == Shape8Kind::kDeep)
+        return fused ? launch_int8_t<G, true, Shape8Deep>(mk, mv, kp, grid, stream)
+                     : launch_int8_t<G, false, Shape8Deep>(mk, mv, kp, grid, stream);
+    return fused ? launch_int8_t<G, true, Shape8Short>(mk, mv, kp, grid, stream)
+                 : launch_int8_t<G, false, Shape8Short>(mk, mv, kp, grid, stream);
 }
 
 } // namespace
@@ -762,11 +779,20 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
         kp.eps = a.eps;
         kp.freqs = make_rope_freqs(a.rope_theta);
     }
-    // long partitions take the 12-warp shape (fold-bound), short ones 9 warps
-    const bool deep = static_cast<long>(a.pages_per_part) * a.page_size >= kDeepChunks8 * kChunkTokens;
-    kp.fused_merge = (deep ? merges_in_kernel<12>(G, a.num_partitions) : merges_in_kernel<9>(G, a.num_partitions))
-                         ? 1
-                         : 0;
+    // Grids of more than one wave (of one CTA per SM) with short partitions
+    // take the two-CTA shape (the fused step and attention alone alike, so
+    // they give equal bits); otherwise long partitions take the 12-warp shape
+    // (fold-bound), short ones 9 warps.
+    const long part_positions = static_cast<long>(a.pages_per_part) * a.page_size;
+    const bool pair = G <= Shape8Pair::kWarps && a.num_partitions > 1 && part_positions <= kPairMaxPositions8 &&
+                      static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);
+    const Shape8Kind shape = pair ? Shape8Kind::kPair
+                             : part_positions >= kDeepChunks8 * kChunkTokens ? Shape8Kind::kDeep
+                                                                             : Shape8Kind::kShort;
+    const bool in_kernel = shape == Shape8Kind::kPair   ? merges_in_kernel<Shape8Pair>(G, a.num_partitions)
+                           : shape == Shape8Kind::kDeep ? merges_in_kernel<Shape8Deep>(G, a.num_partitions)
+                                                        : merges_in_kernel<Shape8Short>(G, a.num_partitions);
+    kp.fused_merge = in_kernel ? 1 : 0;
     if (a.num_partitions > 1) {
         const size_t n = static_cast<size_t>(a.B) * a.Hq * a.num_partitions;
         const auto align256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -779,14 +805,14 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
     switch (G) {
-    case 1: err = launch_int8_g<1>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 2: err = launch_int8_g<2>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 3: err = launch_int8_g<3>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 4: err = launch_int8_g<4>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 5: err = launch_int8_g<5>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 6: err = launch_int8_g<6>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 7: err = launch_int8_g<7>(mk, mv, kp, grid, a.fused, deep, stream); break;
-    case 8: err = launch_int8_g<8>(mk, mv, kp, grid, a.fused, deep, stream); break;
+    case 1: err = launch_int8_g<1>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 2: err = launch_int8_g<2>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 3: err = launch_int8_g<3>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 4: err = launch_int8_g<4>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 5: err = launch_int8_g<5>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 6: err = launch_int8_g<6>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 7: err = launch_int8_g<7>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 8: err = launch_int8_g<8>(mk, mv, kp, grid, a.fused, shape, stream); break;
     default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)

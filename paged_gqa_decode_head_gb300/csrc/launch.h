@@ -117,6 +117,7 @@ struct DecodeInt8Args {
     float *out_f32;
     pgqa_bf16 *out_bf16;
     float *ws;
+    int sm_count; // SMs of the device (selects the CTA shape)
     // fused decode step (decode_step_paged_int8): the prologue runs in the
     // attention kernel; q is unused, the caches are written
     bool fused;

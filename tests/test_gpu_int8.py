@@ -286,6 +286,35 @@ def test_int8_fused_step_matches_the_oracle(num_partitions):
     assert pg.device_error_flags() == 0
 
 
+@pytest.mark.parametrize("Hq,num_partitions", [(8, 64), (24, 32), (48, 40)])
+def test_int8_two_cta_shape(Hq, num_partitions):
+    """Several waves of short partitions (8 sequences x 8 KV heads x 32-64
+    partitions of 32-64 positions) run the two-CTA shape, 6 warps: g = 1, 3
+    and 6; (48, 40) merges in merge_kernel, the others in the last CTA.
+    Attention against the oracle's INT8 attention, the fused step against the
+    oracle's chain and bit for bit against the two launches."""
+    ctx = [2048, 1, 2, 1500, 2047, 700, 2048, 33]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    max_pages = 128
+    np_used = pg.decode_attn_partition_count(len(ctx), 8, 16, max_pages, num_partitions)
+    assert len(ctx) * 8 * np_used > sms and -(-max_pages // np_used) * 16 <= 2048
+    kv = inputs.paged_kv(1400 + Hq, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    assert kv.max_pages == max_pages
+    check_attention(kv, inputs.query(1400 + Hq, len(ctx), Hq), num_partitions)
+    res, kv, tok, (k8, v8, ks, vs) = _fused_vs_two_launch(1410 + Hq, ctx, Hq, num_partitions)
+    for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
+        assert np.array_equal(a, b, equal_nan=False), name
+    q_ref, k8r, v8r, ksr, vsr = oracle.qk_norm_rope_append_int8(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
+                                                                 kv.context_lens, kv.block_table, k8, v8, ks, vs,
+                                                                 16, THETA)
+    ref = oracle.decode_attention_int8(q_ref, k8r, v8r, ksr, vsr, kv.block_table, kv.context_lens, SCALE)
+    gk8, gv8, gks, gvs, gq, of, ob = res["fused"]
+    assert np.abs(of - ref).max() <= ATOL_F32
+    own = oracle.decode_attention_int8(gq, gk8, gv8, gks, gvs, kv.block_table, kv.context_lens, SCALE)
+    assert_bf16_close(ob, oracle.round_bf16(own), "out_bf16")
+    assert pg.device_error_flags() == 0
+
+
 def test_int8_fused_step_flags_empty_context_and_bad_page():
     """T = 0 cannot hold the new token: zeros and the context flag. A new
     position whose page lies outside the pool is not written: page flag."""

@@ -507,14 +507,18 @@ def run_secondary(args):
         ks = torch.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
         vs = torch.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
         int8_bytes = kv_bytes // 512 * (2 * 128 + 2 * 4)
-        n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, 0)
-        ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
-        s = timed(lambda: pg.decode_attn_paged_int8(qd, k8, v8, ks, vs, bt, ctx, scale, out_f32=out, workspace=ws))
-        emit(f"decode_attn_paged_int8 NP={pg.decode_attn_partition_count(B, Hkv, kv.page_size, kv.max_pages, 0)} "
-             "(automatic)", int8_bytes, s, peak, "GB/s", peak_kind,
-             {"bf16_equivalent_gbs": kv_bytes / s / 1e9,
-              "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "int8_bytes": int8_bytes,
-                         "l2": "inputs larger than L2"}})
+        for npr in nps:
+            n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, npr)
+            ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+            np_used = pg.decode_attn_partition_count(B, Hkv, kv.page_size, kv.max_pages, npr)
+            s = timed(lambda: pg.decode_attn_paged_int8(qd, k8, v8, ks, vs, bt, ctx, scale, out_f32=out,
+                                                        workspace=ws, num_partitions=npr))
+            emit(f"decode_attn_paged_int8 NP={np_used}" +
+                 (" (automatic)" if npr == 0 else " (workload's 512-position partitions)"),
+                 int8_bytes, s, peak, "GB/s", peak_kind,
+                 {"bf16_equivalent_gbs": kv_bytes / s / 1e9,
+                  "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "int8_bytes": int8_bytes,
+                             "l2": "inputs larger than L2"}})
         assert pg.device_error_flags() == 0
         return
 

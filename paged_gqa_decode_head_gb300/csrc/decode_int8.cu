@@ -13,9 +13,9 @@
 //
 // GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
 // kW-th 16-position chunk of the partition and a private ring of stages (9
-// warps x 6 stages for short partitions, 12 warps x 4 for long ones, and two
-// CTAs per SM of 6 warps x 4 for grids of several waves with short
-// partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
+// warps x 6 stages for short partitions, 12 warps x 4 for long ones, and
+// three or two CTAs per SM of 4 or 6 warps x 4 for grids of several waves
+// with short partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
 // 128-byte swizzle) plus the chunk's 2 x 64 bytes of scales by bulk copy, all
 // completing on one mbarrier. The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
 // converted in registers: ldmatrix hands a lane four consecutive bytes of a
@@ -94,12 +94,17 @@ using Shape8Short = Shape8<9, 6, 1>;
 // warps leave one of them with three), which long partitions, bound by the
 // fold, need.
 using Shape8Deep = Shape8<12, 4, 1>;
-// Two CTAs per SM of 6 warps x 4 stages (about 100 KiB each) for grids of
-// several waves with short partitions: one CTA's start and end overlap the
-// other's streaming.
+// Grids of several waves with short partitions run several CTAs per SM, so
+// that one CTA's start (table and context loads, first request) and end
+// (merge, state write) overlap the others' streaming: three of 4 warps x 4
+// stages (about 70 KiB each) for partitions up to 1024 positions, two of 6
+// warps x 4 stages (about 105 KiB) up to 2048. B = 1, Hq = 32, T = 131072
+// (us, two / three CTAs per SM): 512-position partitions 76.9 / 66.3, 1024
+// 65.2 / 61.0, 2048 60.4 / 68.8.
 using Shape8Pair = Shape8<6, 4, 2>;
-// Longest partition (positions) the two-CTA shape takes.
+using Shape8Trio = Shape8<4, 4, 3>;
 constexpr int kPairMaxPositions8 = 2048;
+constexpr int kTrioMaxPositions8 = 1024;
 
 struct Int8Params {
     const uint16_t *q;
@@ -715,12 +720,17 @@ template <typename S> bool merges_in_kernel(int G, int num_partitions)
            static_cast<long>(G) * num_partitions * kHeadDim * 4 + S::kMergeScratch <= S::kStageArea;
 }
 
-enum class Shape8Kind { kShort, kDeep, kPair };
+enum class Shape8Kind { kShort, kDeep, kPair, kTrio };
 
 template <int G>
 cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
                           bool fused, Shape8Kind shape, cudaStream_t stream)
 {
+    if constexpr (G <= Shape8Trio::kWarps) {
+        if (shape == Shape8Kind::kTrio)
+            return fused ? launch_int8_t<G, true, Shape8Trio>(mk, mv, kp, grid, stream)
+                         : launch_int8_t<G, false, Shape8Trio>(mk, mv, kp, grid, stream);
+    }
     if constexpr (G <= Shape8Pair::kWarps) {
         if (shape == Shape8Kind::kPair)
             return fused ? launch_int8_t<G, true, Shape8Pair>(mk, mv, kp, grid, stream)
@@ -780,16 +790,19 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
         kp.freqs = make_rope_freqs(a.rope_theta);
     }
     // Grids of more than one wave (of one CTA per SM) with short partitions
-    // take the two-CTA shape (the fused step and attention alone alike, so
-    // they give equal bits); otherwise long partitions take the 12-warp shape
-    // (fold-bound), short ones 9 warps.
+    // take three or two CTAs per SM (the fused step and attention alone
+    // alike, so they give equal bits); otherwise long partitions take the
+    // 12-warp shape (fold-bound), short ones 9 warps.
     const long part_positions = static_cast<long>(a.pages_per_part) * a.page_size;
-    const bool pair = G <= Shape8Pair::kWarps && a.num_partitions > 1 && part_positions <= kPairMaxPositions8 &&
-                      static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);
-    const Shape8Kind shape = pair ? Shape8Kind::kPair
-                             : part_positions >= kDeepChunks8 * kChunkTokens ? Shape8Kind::kDeep
-                                                                             : Shape8Kind::kShort;
-    const bool in_kernel = shape == Shape8Kind::kPair   ? merges_in_kernel<Shape8Pair>(G, a.num_partitions)
+    const bool waves = a.num_partitions > 1 &&
+                       static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);
+    Shape8Kind shape = part_positions >= kDeepChunks8 * kChunkTokens ? Shape8Kind::kDeep : Shape8Kind::kShort;
+    if (waves && G <= Shape8Trio::kWarps && part_positions <= kTrioMaxPositions8)
+        shape = Shape8Kind::kTrio;
+    else if (waves && G <= Shape8Pair::kWarps && part_positions <= kPairMaxPositions8)
+        shape = Shape8Kind::kPair;
+    const bool in_kernel = shape == Shape8Kind::kTrio   ? merges_in_kernel<Shape8Trio>(G, a.num_partitions)
+                           : shape == Shape8Kind::kPair ? merges_in_kernel<Shape8Pair>(G, a.num_partitions)
                            : shape == Shape8Kind::kDeep ? merges_in_kernel<Shape8Deep>(G, a.num_partitions)
                                                         : merges_in_kernel<Shape8Short>(G, a.num_partitions);
     kp.fused_merge = in_kernel ? 1 : 0;

@@ -287,10 +287,11 @@ def test_int8_fused_step_matches_the_oracle(num_partitions):
 
 
 @pytest.mark.parametrize("Hq,num_partitions", [(8, 64), (24, 32), (48, 40)])
-def test_int8_two_cta_shape(Hq, num_partitions):
+def test_int8_several_ctas_per_sm(Hq, num_partitions):
     """Several waves of short partitions (8 sequences x 8 KV heads x 32-64
-    partitions of 32-64 positions) run the two-CTA shape, 6 warps: g = 1, 3
-    and 6; (48, 40) merges in merge_kernel, the others in the last CTA.
+    partitions of 32-64 positions) run several CTAs per SM: three of 4 warps
+    for g = 1 and 3, two of 6 warps for g = 6 (which merges in merge_kernel;
+    the others merge in the last CTA).
     Attention against the oracle's INT8 attention, the fused step against the
     oracle's chain and bit for bit against the two launches."""
     ctx = [2048, 1, 2, 1500, 2047, 700, 2048, 33]

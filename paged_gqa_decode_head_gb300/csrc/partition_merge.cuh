@@ -98,6 +98,10 @@ __device__ bool merge_partitions_in_cta(const float *ws_m, const float *ws_l, co
         if (item < kItems && slice < kSlices) {
             const int h = item / 32, d4 = item % 32;
             const float4 *src = reinterpret_cast<const float4 *>(acc + static_cast<size_t>(h) * n * kHeadDim) + d4;
+            // unrolled so that several partitions' loads are in flight at
+            // once (the sum's order is unchanged): M = 4 fused step 11.19 ->
+            // 11.09 us per layer
+#pragma unroll 4
             for (int part = slice; part < n; part += kSlices) {
                 const float4 v = src[static_cast<size_t>(part) * (kHeadDim / 4)];
                 const float wt = w[h * kMaxParts + part];

@@ -169,7 +169,14 @@ size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, 
  * that kernel completes. The previous kernel must therefore not write those
  * inputs (qk_norm_rope_append does not).
  *   num_partitions  0 = automatic, else the requested NP.
- * A sequence with T_b = 0 produces zeros.
+ * A sequence with T_b = 0 produces zeros. For given arguments on a given
+ * device the results are reproducible bit for bit: the partition count, the
+ * kernel's CTA shape (one CTA per SM, or two smaller ones for grids of more
+ * than one wave whose partitions are at most 2048 positions) and every
+ * summation order depend only on them and on the device's SM count. Up to
+ * 64 partitions whose states fit the CTA's shared memory are merged by the
+ * last CTA of each (sequence, KV head); otherwise a merge kernel follows in
+ * the same stream.
  */
 int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
                       const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
@@ -278,8 +285,11 @@ int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const 
  *   Reading and PDL rules as decode_attn_paged; workspace of
  *   decode_attn_int8_workspace_size bytes with decode_attn_paged's rules
  *   (zero-filled before the first call with given arguments, left ready by
- *   every completed call, not shared by calls that may overlap); with up to
- *   64 partitions the last CTA of each (sequence, KV head) merges them.
+ *   every completed call, not shared by calls that may overlap); up to 64
+ *   partitions whose states fit the CTA's shared memory are merged by the
+ *   last CTA of each (sequence, KV head), more by a merge kernel in the same
+ *   stream. The CTA shape follows the sizes as for decode_attn_paged (one,
+ *   two or three CTAs per SM), so results are reproducible per device.
  */
 int qk_norm_rope_append_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
                              const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,

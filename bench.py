@@ -39,6 +39,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention KV GB/s (fraction of HBM peak); µs per layer-step at T=8K"
 WORKLOAD = "qwen3_0p6b_t8k"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_step_kernel_qwen3_t8k.md")
+# GB300's nominal HBM3e bandwidth, reported beside the measured copy peak
+NOMINAL_HBM_GBS = 7900.0
 
 
 def parse_args():
@@ -411,6 +413,7 @@ def run_ours(args, rank, world, local):
                    "l2": "inputs larger than L2: 896 MiB of KV, each layer's 32 MiB read once per step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": profiled_traffic(),
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "kernel": "decode_mma_kernel<2, fused> (decode_step_paged: prologue, split-KV attention, "
                                f"in-kernel merge), {n_layers} launches per step graph, CUDA events on the launch "
                                "stream; achieved = algorithmic bytes of one launch / (step time / launches)",
@@ -473,6 +476,8 @@ def run_secondary(args):
                 "workload": args.workload, "variant": variant, "steps": iters, "data": "synthetic",
                 "roofline": {"achieved": gbs, "peak": roof_peak, "unit": roof_unit, "frac": gbs / roof_peak,
                              "peak_kind": roof_kind}}
+        if roof_unit == "GB/s" and roof_kind != "measured link":
+            line["roofline"]["frac_of_nominal"] = gbs / NOMINAL_HBM_GBS
         line.update(extra)
         print(json.dumps(line), flush=True)
 

@@ -228,22 +228,48 @@ def oracle_layer(layer, theta):
     oracle.decode_attention(q_ref, kc, vc, kv.block_table, kv.context_lens, 1.0 / math.sqrt(128))
 
 
-def time_oracle(layers, theta, n_layer_evals: int):
-    """Run the oracle's prologue + attention on n_layer_evals layers (cycling
-    through the step's layers) on all host cores; returns (seconds, cores)."""
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def run_oracle_jobs(jobs, threads: int) -> float:
+    """Run the callables on `threads` host threads (ctypes releases the GIL);
+    returns the wall time in seconds."""
+    t0 = time.perf_counter()
+    if threads <= 1:
+        for fn in jobs:
+            fn()
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda fn: fn(), jobs))
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(jobs, single_jobs, unit_bytes, single_bytes, sample: str, single_sample: str) -> dict:
+    """The fp64 oracle timed on the host: `jobs` spread over all host cores
+    (one thread per job at most) and `single_jobs` on one thread. Returns the
+    cpu_baseline record (GB/s of KV the oracle gets through)."""
     import oracle
 
     oracle.build()
-    cores = len(os.sched_getaffinity(0))
-    jobs = [layers[i % len(layers)] for i in range(n_layer_evals)]
-    t0 = time.perf_counter()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as ex:  # ctypes releases the GIL
-        list(ex.map(lambda lay: oracle_layer(lay, theta), jobs))
-    return time.perf_counter() - t0, min(cores, n_layer_evals)
+    threads = min(host_cores(), len(jobs))
+    s_all = run_oracle_jobs(jobs, threads)
+    s_one = run_oracle_jobs(single_jobs, 1)
+    return {"value": unit_bytes / s_all / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{sample}, spread over {threads} host threads",
+            "single_thread": {"value": single_bytes / s_one / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": single_sample}}
 
 
 def kv_bytes_layer(T, Hkv=8, D=128):
     return 4 * T * Hkv * D
+
+
+def headline_config(w, n_layers: int) -> dict:
+    """The workload of the headline line, the same for both arms."""
+    return {"workload": WORKLOAD, "layers": n_layers, "B": w["B"], "Hq": w["Hq"], "Hkv": w["Hkv"], "D": 128,
+            "T": w["T"], "page_size": w["page_size"],
+            "l2": "inputs larger than L2: 896 MiB of KV, each layer's 32 MiB read once per step"}
 
 
 def run_reference(args, rank, world):
@@ -251,29 +277,30 @@ def run_reference(args, rank, world):
         return
     from paged_gqa_decode_head_gb300 import inputs
 
+    import oracle
+
+    oracle.build()
     w = inputs.WORKLOADS[WORKLOAD]
     n_layers = args.layers or w["layers"]
     layers = inputs.qwen3_layers(layers=n_layers)
-    sample_layers = min(n_layers, 8)  # one step of the reference arm = 8 of the 28 layers
+    jobs = [lambda lay=lay: oracle_layer(lay, w["theta"]) for lay in layers]
+    threads = min(host_cores(), len(jobs))
     for _ in range(args.warmup):
-        time_oracle(layers, w["theta"], sample_layers)
+        run_oracle_jobs(jobs, threads)
     total_s = 0.0
-    cores = 1
     for _ in range(args.steps):
-        s, cores = time_oracle(layers, w["theta"], sample_layers)
-        total_s += s
-    layer_s = total_s / (args.steps * sample_layers)
-    gbs = kv_bytes_layer(w["T"]) / layer_s / 1e9
-    sample = (f"{sample_layers} of the {n_layers} layers per step (prologue + full-softmax attention, T={w['T']}), "
-              f"fp64 oracle, layers spread over {cores} host threads")
+        total_s += run_oracle_jobs(jobs, threads)
+    step_s = total_s / args.steps
+    gbs = kv_bytes_layer(w["T"]) * n_layers / step_s / 1e9
+    sample = (f"one whole step per timed step: all {n_layers} layers (prologue + full-softmax attention, T={w['T']}), "
+              f"fp64 oracle, layers spread over {threads} host threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "us_per_layer_step": layer_s * 1e6,
-        "config": {"workload": WORKLOAD, "layers": n_layers, "B": 1, "Hq": 16, "Hkv": 8, "D": 128, "T": w["T"],
-                   "page_size": 16},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "us_per_layer_step": step_s * 1e6 / n_layers,
+        "config": headline_config(w, n_layers),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -305,12 +332,12 @@ def run_ours(args, rank, world, local):
     # CPU-baseline leg first (rank 0, one GPU job only), before any GPU work
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample_layers = n_layers
-        s, cores = time_oracle(layers, w["theta"], sample_layers)
-        gbs = kv_bytes_layer(w["T"]) * sample_layers / s / 1e9
-        cpu_baseline = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                        "sample": f"one full step ({sample_layers} layers, prologue + full-softmax attention, "
-                                  f"T={w['T']}) of the fp64 oracle, layers spread over {cores} host threads"}
+        jobs = [lambda lay=lay: oracle_layer(lay, w["theta"]) for lay in layers]
+        n_single = min(4, n_layers)
+        cpu_baseline = oracle_baseline(
+            jobs, jobs[:n_single], kv_bytes_layer(w["T"]) * n_layers, kv_bytes_layer(w["T"]) * n_single,
+            f"one whole step ({n_layers} layers, prologue + full-softmax attention, T={w['T']}) of the fp64 oracle",
+            f"{n_single} of the step's layers one after another on one host thread")
 
     step = DecodeStep(layers, Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"], device=dev)
     np_used = step.partitions
@@ -403,14 +430,15 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32", "storage_dtype": "bf16", "accumulate": "f32",
+        "p_operand": "bf16 hi + lo pair (about 16 significant bits) in the P.V product; scores and sums in f32",
+        "data": "synthetic",
         "us_per_layer_step": step_s * 1e6 / n_layers,
         "attention_us_per_layer": layer_attn_s * 1e6,
         "two_launch_us_per_layer_step": ms_two / args.steps / n_layers * 1e3,
         "hbm_fraction_of_step": value / world / peak,
-        "config": {"workload": WORKLOAD, "layers": n_layers, "B": 1, "Hq": w["Hq"], "Hkv": w["Hkv"], "D": 128,
-                   "T": w["T"], "page_size": 16, "num_partitions": np_used, "graph": "one CUDA graph per step",
-                   "l2": "inputs larger than L2: 896 MiB of KV, each layer's 32 MiB read once per step"},
+        "config": headline_config(w, n_layers),
+        "launch": {"num_partitions": np_used, "graph": f"one CUDA graph per step ({n_layers} launches)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": profiled_traffic(),
                      "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
@@ -449,13 +477,18 @@ def run_secondary(args):
     from paged_gqa_decode_head_gb300 import inputs
     from paged_gqa_decode_head_gb300.runner import to_device_bf16, to_device_i32
 
+    import oracle
+
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    idle = gpu_idle_check(smi_gpu_id(dev))
     pg.load_library()
     w = inputs.WORKLOADS[args.workload]
     scale = 1.0 / math.sqrt(128)
     peak, peak_kind = load_peaks()
     iters = max(3, min(args.steps, 500))
+    sampler = ClockSampler(smi_gpu_id(dev))
+    state = {"cpu": None}
 
     def timed(fn):
         for _ in range(max(3, args.warmup)):
@@ -463,11 +496,13 @@ def run_secondary(args):
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        state["t0"] = time.time()
         e0.record()
         for _ in range(iters):
             fn()
         e1.record()
         torch.cuda.synchronize(dev)
+        state["t1"] = time.time()
         return e0.elapsed_time(e1) / iters / 1e3
 
     def emit(variant, nbytes, s, roof_peak, roof_unit, roof_kind, extra):
@@ -475,19 +510,48 @@ def run_secondary(args):
         line = {"metric": f"{args.workload} {variant}", "value": gbs, "unit": "GB/s", "us": s * 1e6,
                 "workload": args.workload, "variant": variant, "steps": iters, "data": "synthetic",
                 "roofline": {"achieved": gbs, "peak": roof_peak, "unit": roof_unit, "frac": gbs / roof_peak,
-                             "peak_kind": roof_kind}}
+                             "peak_kind": roof_kind, "bytes": nbytes}}
         if roof_unit == "GB/s" and roof_kind != "measured link":
             line["roofline"]["frac_of_nominal"] = gbs / NOMINAL_HBM_GBS
         line.update(extra)
+        line["clocks"] = sampler.summary(state["t0"], state["t1"])
+        line["gpu_idle_at_start"] = idle
+        line["cpu_baseline"] = state["cpu"]
         print(json.dumps(line), flush=True)
+
+    def baseline(jobs, n_single, bytes_of, sample, single_sample):
+        """The oracle on the same inputs, before any GPU timing (skipped with
+        --no-cpu-baseline)."""
+        if args.no_cpu_baseline:
+            return
+        state["cpu"] = oracle_baseline(jobs, jobs[:n_single], sum(bytes_of), sum(bytes_of[:n_single]), sample,
+                                       single_sample)
 
     if args.workload in ("ragged_b64", "long_split_kv_t128k"):
         if args.workload == "ragged_b64":
             kv, q = inputs.ragged_b64()
             nps = [0]
+            jobs = [lambda b=b: oracle.decode_attention(q[b:b + 1], kv.k_cache, kv.v_cache, kv.block_table[b:b + 1],
+                                                        kv.context_lens[b:b + 1], scale)
+                    for b in range(len(kv.context_lens))]
+            sizes = [kv_bytes_layer(int(t), w["Hkv"]) for t in kv.context_lens]
+            baseline(jobs, 8, sizes, f"all {len(jobs)} sequences of the batch, full-softmax attention",
+                     "the first 8 sequences one after another on one host thread")
         else:
             kv, q = inputs.long_split_kv()
             nps = [w["T"] // w["partition"], 0]
+            g = w["Hq"] // w["Hkv"]
+            # one job per KV head (its group of query heads over its own copy of that head's cache)
+            heads = [(q[:, h * g:(h + 1) * g].copy(), kv.k_cache[:, h:h + 1].copy(), kv.v_cache[:, h:h + 1].copy())
+                     for h in range(w["Hkv"])]
+            jobs = [lambda x=x: oracle.decode_attention(x[0], x[1], x[2], kv.block_table, kv.context_lens, scale)
+                    for x in heads]
+            baseline(jobs, 1, [kv_bytes_layer(w["T"], 1)] * len(jobs),
+                     f"the whole T={w['T']} attention, one job per KV head (its {g} query heads)",
+                     "one KV head's job on one host thread")
+            del heads
+        sampler.start()
+        time.sleep(0.5)
         B, Hq, Hkv = len(kv.context_lens), w["Hq"], w["Hkv"]
         qd = to_device_bf16(q, dev)
         kc, vc = to_device_bf16(kv.k_cache, dev), to_device_bf16(kv.v_cache, dev)
@@ -524,6 +588,7 @@ def run_secondary(args):
                  {"bf16_equivalent_gbs": kv_bytes / s / 1e9,
                   "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "P": kv.page_size, "int8_bytes": int8_bytes,
                              "l2": "inputs larger than L2"}})
+        sampler.stop()
         assert pg.device_error_flags() == 0
         return
 
@@ -532,6 +597,19 @@ def run_secondary(args):
         # M-token attention, 28 layers in one CUDA graph
         layers = inputs.qwen3_layers_multi()
         B, M, Hq, Hkv, T = w["B"], w["M"], w["Hq"], w["Hkv"], w["T"]
+
+        def oracle_multi(layer):
+            kv, q, k, v, gq, gk = layer
+            q_ref, kc, vc = oracle.qk_norm_rope_append_multi(q, k, v, gq, gk, kv.context_lens, kv.block_table,
+                                                             kv.k_cache, kv.v_cache, kv.page_size, w["theta"])
+            oracle.decode_attention_multi(q_ref, kc, vc, kv.block_table, kv.context_lens, scale)
+
+        jobs = [lambda lay=lay: oracle_multi(lay) for lay in layers]
+        baseline(jobs, 2, [kv_bytes_layer(T, Hkv)] * len(jobs),
+                 f"one whole step ({len(jobs)} layers, M={M}-token prologue + full-softmax attention)",
+                 "2 of the step's layers one after another on one host thread")
+        sampler.start()
+        time.sleep(0.5)
         bufs = []
         for kv, q, k, v, gq, gk in layers:
             bufs.append(dict(kc=to_device_bf16(kv.k_cache, dev), vc=to_device_bf16(kv.v_cache, dev),
@@ -578,6 +656,7 @@ def run_secondary(args):
                   "config": {"B": B, "M": M, "Hq": Hq, "Hkv": Hkv, "T": T, "P": P, "layers": L,
                              "num_partitions": pg.decode_attn_partition_count(B, Hkv, P, max_pages, 0),
                              "l2": "inputs larger than L2: 896 MiB of KV"}})
+        sampler.stop()
         assert pg.device_error_flags() == 0
         return
 
@@ -587,13 +666,18 @@ def run_secondary(args):
         B, Hq, Hkv, T = w["B"], w["Hq"], w["Hkv"], w["T"]
         L = 28
         bufs = []
+        host = []
         for i in range(L):
             seed = w["seed"] * 1000 + i
             kv = inputs.paged_kv(seed, [T] * B, Hkv=Hkv, page_size=w["page_size"], spare_pages=0,
                                  fill_unused="normal")
             tok = inputs.new_token(seed, B, Hq, Hkv)
-            k8 = torch.from_numpy(inputs.int8_rows(seed, kv.k_cache.shape, 70)).to(dev)
-            v8 = torch.from_numpy(inputs.int8_rows(seed, kv.v_cache.shape, 71)).to(dev)
+            k8h = inputs.int8_rows(seed, kv.k_cache.shape, 70)
+            v8h = inputs.int8_rows(seed, kv.v_cache.shape, 71)
+            if i < 8:
+                host.append((kv, tok, k8h, v8h))
+            k8 = torch.from_numpy(k8h).to(dev)
+            v8 = torch.from_numpy(v8h).to(dev)
             ks = torch.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
             vs = torch.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device=dev)
             bufs.append(dict(k8=k8, v8=v8, ks=ks, vs=vs, bt=to_device_i32(kv.block_table, dev),
@@ -605,6 +689,23 @@ def run_secondary(args):
                              P=kv.page_size, mp=kv.max_pages))
         n = pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, bufs[0]["P"], bufs[0]["mp"], 0)
         ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
+
+        def oracle_int8(layer):
+            kv, tok, k8h, v8h = layer
+            ks = np.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=np.float32)
+            vs = np.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=np.float32)
+            q_ref, kc, vc, ksc, vsc = oracle.qk_norm_rope_append_int8(
+                tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k, kv.context_lens, kv.block_table, k8h, v8h, ks, vs,
+                kv.page_size, w["theta"])
+            oracle.decode_attention_int8(q_ref, kc, vc, ksc, vsc, kv.block_table, kv.context_lens, scale)
+
+        jobs = [lambda lay=lay: oracle_int8(lay) for lay in host]
+        baseline(jobs, 2, [(2 * 128 + 2 * 4) * T * Hkv] * len(jobs),
+                 f"{len(jobs)} of the step's {L} layers (INT8 prologue + full-softmax attention over the codes)",
+                 "2 layers one after another on one host thread")
+        del host
+        sampler.start()
+        time.sleep(0.5)
 
         def attention_only():
             for b_ in bufs:
@@ -646,12 +747,22 @@ def run_secondary(args):
                   "config": {"B": B, "Hq": Hq, "Hkv": Hkv, "T": T, "P": bufs[0]["P"], "layers": L,
                              "bytes_per_row": "128 int8 codes + 1 float scale, K and V",
                              "l2": "inputs larger than L2: 462 MB of int8 KV"}})
+        sampler.stop()
         assert pg.device_error_flags() == 0
         return
 
     # host_tiled_t64k: the copy pipeline and the zero-copy variant
     q, k, v = inputs.host_tiled_kv()
     B, Hq, Hkv, T, tile = w["B"], w["Hq"], w["Hkv"], w["T"], w["tile"]
+    g = Hq // Hkv
+    heads = [(q[:, h * g:(h + 1) * g].copy(), k[:, :, h:h + 1].copy(), v[:, :, h:h + 1].copy()) for h in range(Hkv)]
+    jobs = [lambda x=x: oracle.attention_contiguous(x[0], x[1], x[2], scale) for x in heads]
+    baseline(jobs, 1, [kv_bytes_layer(T, 1) * B] * len(jobs),
+             f"the whole T={T} attention, one job per KV head (its {g} query heads)",
+             "one KV head's job on one host thread")
+    del heads
+    sampler.start()
+    time.sleep(0.5)
     hk = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).pin_memory()
     hv = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory()
     nbytes = 2 * hk.numel() * 2
@@ -686,6 +797,7 @@ def run_secondary(args):
     np_used = pg.attn_host_direct_partition_count(B, Hkv, T, 0)
     s = timed(lambda: pg.attn_host_direct(qd, hk, hv, scale, out_f32=out, workspace=ws))
     emit(f"attn_host_direct (zero-copy, NP={np_used})", nbytes, s, link, "GB/s", "measured link", {"config": cfg})
+    sampler.stop()
 
 
 def main():

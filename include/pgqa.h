@@ -436,8 +436,11 @@ int attn_host_direct(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf1
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  *
  * The first call on each device (that needs scratch) looks the array's
- * device address up with cudaGetSymbolAddress; make that first call before
- * any stream capture on that device. All calls share the one array, which
+ * device address up with cudaGetSymbolAddress and keeps it with the id of
+ * the device's current context; the first call after that context is torn
+ * down and made again (cudaDeviceReset) looks it up again. Make the first
+ * call on a device, and the first after a reset, before any stream capture
+ * on that device. All calls share the one array, which
  * keeps the last call's contents: each call first clears the part that must
  * start at zero (the partition tickets) with cudaMemsetAsync on `stream`.
  * Calls whose work overlaps on the GPU (different streams, or no ordering

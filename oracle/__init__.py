@@ -50,8 +50,6 @@ def _load():
         lib.oracle_bf16_to_double.restype = D
         lib.oracle_round_bf16.argtypes = [D]
         lib.oracle_round_bf16.restype = ctypes.c_uint16
-        lib.oracle_round_f32.argtypes = [D]
-        lib.oracle_round_f32.restype = ctypes.c_float
         lib.oracle_head_rmsnorm.argtypes = [P, P, I, D, P]
         lib.oracle_head_rmsnorm.restype = None
         lib.oracle_rope_half.argtypes = [P, I, L, D, P]
@@ -141,11 +139,6 @@ def round_bf16(x) -> np.ndarray:
     flat = a.reshape(-1)
     out = np.fromiter((lib.oracle_round_bf16(float(v)) for v in flat), dtype=np.uint16, count=flat.size)
     return out.reshape(a.shape)
-
-
-def round_f32(x) -> np.ndarray:
-    a = np.asarray(x, dtype=np.float64)
-    return a.astype(np.float32)
 
 
 # --------------------------------------------------------------------------

@@ -88,9 +88,6 @@ uint16_t oracle_round_bf16(double x)
     return (uint16_t)(sign | (uint16_t)(u >> 16));
 }
 
-/* Round a double to binary32 (C conversion, round-to-nearest-even). */
-float oracle_round_f32(double x) { return (float)x; }
-
 /* ------------------------------------------------------------------------- */
 /* A3: per-head RMSNorm [Qwen3 runtime s2.1 definition, s2.3 per head]       */
 /* ------------------------------------------------------------------------- */

@@ -817,7 +817,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     if (p.context_lens) {
         const int b = row / (p.M * p.Hq);
         int T = p.context_lens[b];
-        if (T < 0 || T > p.max_pages * p.P)
+        // the split kernel's test of a bad context (M new tokens need T >= M)
+        if (T < (p.M > 1 ? p.M : 0) || T > p.max_pages * p.P)
             T = 0;
         const int part_tokens = p.ppp * p.P;
         np = min(np, max(1, (T + part_tokens - 1) / part_tokens));

@@ -11,9 +11,16 @@
 // The scratch is a file-scope __device__ array of kStaticScratchBytes. Every
 // GPU that loads this library holds it until the process exits. Host code
 // cannot use the array's name as a device address (on the host it names a
-// stand-in object), so the device address is looked up once per device with
-// cudaGetSymbolAddress and passed to the kernels as an ordinary pointer.
+// stand-in object), so the device address is looked up with
+// cudaGetSymbolAddress and passed to the kernels as an ordinary pointer. The
+// lookup is set-up work done once per device and context: the address is
+// kept together with the unique id of the context it was found in
+// (cuCtxGetId), so a context torn down and made again (cudaDeviceReset),
+// which may load the array elsewhere, gets a fresh lookup instead of a stale
+// address.
 #include <mutex>
+
+#include <cuda.h>
 
 #include "launch.h"
 #include "pgqa.h"
@@ -25,11 +32,44 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 
-// Device address of the scratch array on the current device, looked up on the
-// first call for that device.
+struct ScratchSlot {
+    unsigned long long ctx_id; // unique id of the context the address belongs to
+    void *ptr;                 // device address of g_static_scratch there, or NULL
+};
+
+std::mutex g_setup_mutex;
+ScratchSlot g_scratch[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (false if there is none
+// or the driver cannot say).
+bool current_context_id(unsigned long long *id)
+{
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array on the current device. The first call
+// on a device, and the first after its context was made again, looks it up.
 cudaError_t scratch_address(void **out)
 {
     int dev = 0;
@@ -39,14 +79,18 @@ cudaError_t scratch_address(void **out)
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
+    if (!known || !g_scratch[dev].ptr || g_scratch[dev].ctx_id != id) {
         void *p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_static_scratch);
+        err = cudaGetSymbolAddress(&p, g_static_scratch); // also makes the context current if needed
         if (err != cudaSuccess)
             return err;
-        g_scratch_ptr[dev] = p;
+        if (!known && !current_context_id(&id))
+            return cudaErrorNotSupported;
+        g_scratch[dev] = ScratchSlot{id, p};
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch[dev].ptr;
     return cudaSuccess;
 }
 
@@ -72,7 +116,7 @@ extern "C" int decode_attn_paged_static(const pgqa_bf16 *q, const pgqa_bf16 *k_c
         cudaError_t err = scratch_address(&scratch);
         if (err != cudaSuccess)
             return pgqa::report_error(PGQA_ERR_CUDA,
-                                      "decode_attn_paged_static: cudaGetSymbolAddress failed: %s",
+                                      "decode_attn_paged_static: no device address for the scratch array: %s",
                                       cudaGetErrorString(err));
         // The array keeps whatever the last call left, and a call with other
         // sizes may have left partition data where this call's partition

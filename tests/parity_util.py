@@ -1,9 +1,13 @@
 """Comparison helpers shared by the GPU parity tests.
 
 bf16 bar: the GPU's bf16 result and the oracle's nearest-even rounding of its
-fp64 result may differ by at most 1 bf16 ulp. Below 2^-10 the fp32 arithmetic
-error (about 1e-7 of the inputs' scale), not the cast, sets the achievable
-accuracy, so there the ulp is counted as that of 2^-10 (2^-17 absolute).
+fp64 result may differ by at most 1 bf16 ulp. Below 2^-10 the absolute error
+of the computation, not the cast, sets the achievable accuracy: the attention
+weights p enter the P.V product as a bf16 hi + lo pair (about 16 significant
+bits, relative error up to 2^-17 per weight), which leaves an absolute error
+of order 2^-17 times the magnitude of V on every output; the fp32
+accumulation adds about 1e-7. So there the ulp is counted as that of 2^-10
+(2^-17 absolute).
 """
 import numpy as np
 

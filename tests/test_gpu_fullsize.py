@@ -1,8 +1,11 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
-benchmark times. Where the oracle would be too slow for every output, a
-seeded sample of sequences is checked one by one and properties that hold at
-any size are checked for the rest."""
+benchmark times. Every output element is compared with the fp64 oracle: the
+fp32 outputs within 2e-3, the bf16 outputs within 1 ulp of the oracle's
+nearest-even rounding. The oracle runs one sequence (or layer) per host
+thread; its C routines release the GIL."""
+import concurrent.futures
 import math
+import os
 
 import numpy as np
 import pytest
@@ -20,10 +23,19 @@ ATOL_F32 = 2e-3
 SCALE = 1.0 / math.sqrt(128)
 
 
+def _host_threads():
+    return max(1, len(os.sched_getaffinity(0)))
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_qwen3_28_layer_step_t8192_graph(fused):
     """The benchmark's step (fused: one decode_step_paged launch per layer;
-    otherwise qk_norm_rope_append + decode_attn_paged) replayed as one graph."""
+    otherwise qk_norm_rope_append + decode_attn_paged) replayed as one graph.
+
+    Every layer's outputs are compared with the oracle's whole chain (its own
+    prologue, then attention): fp32 within 2e-3 and bf16 within 1 ulp of the
+    oracle's rounded result, even on layers whose rotated q or appended K
+    differ from the oracle's by their allowed 1 ulp (counted and reported)."""
     w = inputs.WORKLOADS["qwen3_0p6b_t8k"]
     layers = inputs.qwen3_layers()
     step = DecodeStep(layers, Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"])
@@ -31,19 +43,37 @@ def test_qwen3_28_layer_step_t8192_graph(fused):
     step.replay()
     torch.cuda.synchronize()
     assert pg.device_error_flags() == 0
-    worst = 0.0
-    for (kv, tok), st in zip(layers, step.layers):
+
+    def reference(i):
+        kv, tok = layers[i]
         q_ref, kc_ref, vc_ref = oracle.qk_norm_rope_append(tok.q, tok.k, tok.v, tok.gamma_q, tok.gamma_k,
-                                                           kv.context_lens, kv.block_table, kv.k_cache, kv.v_cache,
-                                                           kv.page_size, w["theta"])
-        assert_bf16_close(bf16_bits(st.q_out), q_ref)
+                                                           kv.context_lens, kv.block_table, kv.k_cache,
+                                                           kv.v_cache, kv.page_size, w["theta"])
         ref = oracle.decode_attention(q_ref, kc_ref, vc_ref, kv.block_table, kv.context_lens, SCALE)
-        err = np.abs(st.out_f32.cpu().numpy().astype(np.float64) - ref).max()
+        return q_ref, kc_ref, vc_ref, ref
+
+    with concurrent.futures.ThreadPoolExecutor(_host_threads()) as ex:
+        refs = list(ex.map(reference, range(len(layers))))
+    worst = 0.0
+    exact_prologue = 0
+    for (kv, tok), st, (q_ref, kc_ref, vc_ref, ref) in zip(layers, step.layers, refs):
+        q_bits = bf16_bits(st.q_out)
+        kc_bits = bf16_bits(st.k_cache)
+        assert_bf16_close(q_bits, q_ref, "q_out")
+        assert_bf16_close(kc_bits, kc_ref, "appended K")
+        assert np.array_equal(bf16_bits(st.v_cache), vc_ref)
+        exact_prologue += int(np.array_equal(q_bits, q_ref) and np.array_equal(kc_bits, kc_ref))
+        of = st.out_f32.cpu().numpy().astype(np.float64)
+        ob = bf16_bits(st.out_bf16)
+        err = np.abs(of - ref).max()
         worst = max(worst, err)
         assert err <= ATOL_F32
-        # the bf16 output is the nearest-even cast of the fp32 output
-        assert np.array_equal(bf16_bits(st.out_bf16), oracle.round_bf16(st.out_f32.cpu().numpy()))
-    print(f"28 layers: worst |out - oracle| = {worst:.2e}")
+        # the bf16 output is the nearest-even cast of the fp32 output ...
+        assert np.array_equal(ob, oracle.round_bf16(of))
+        # ... and within 1 ulp of the oracle's chain
+        assert_bf16_close(ob, oracle.round_bf16(ref), "out_bf16 against the oracle's chain")
+    print(f"28 layers: worst |out - oracle| = {worst:.2e}; q_out and appended K bit-equal to the oracle's on "
+          f"{exact_prologue} layers, within 1 ulp on the others")
     # replaying the step reproduces every output bit for bit (the appends
     # rewrite the same rows; the fold grouping never depends on timing)
     first = step.outputs.clone()
@@ -53,7 +83,9 @@ def test_qwen3_28_layer_step_t8192_graph(fused):
     assert torch.equal(step.outputs, first)
 
 
-def test_ragged_b64_full_size_sampled():
+def test_ragged_b64_full_size_every_sequence():
+    """B = 64 ragged contexts in one shared pool, automatic partitions (the
+    benchmark's launch): every sequence against the oracle at both bars."""
     w = inputs.WORKLOADS["ragged_b64"]
     kv, q = inputs.ragged_b64()
     dev = "cuda"
@@ -64,19 +96,24 @@ def test_ragged_b64_full_size_sampled():
     ws = torch.zeros(max(16, pg.decode_attn_workspace_size(B, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, 0)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((B, w["Hq"], 128), dtype=torch.float32, device=dev)
-    pg.decode_attn_paged(qd, kc, vc, bt, ctx, SCALE, out_f32=out, workspace=ws)
+    outb = torch.empty((B, w["Hq"], 128), dtype=torch.bfloat16, device=dev)
+    pg.decode_attn_paged(qd, kc, vc, bt, ctx, SCALE, out_f32=out, out_bf16=outb, workspace=ws)
     torch.cuda.synchronize()
     assert pg.device_error_flags() == 0
-    o = out.cpu().numpy()
-    assert np.isfinite(o).all()
-    # a convex combination of unit-normal V rows stays well inside their range
-    assert np.abs(o).max() < 6.0
-    order = np.argsort(kv.context_lens)
-    sample = sorted({int(order[0]), int(order[-1]), *np.random.default_rng(5).choice(B, 4, replace=False).tolist()})
-    for b in sample:
-        ref = oracle.decode_attention(q[b:b + 1], kv.k_cache, kv.v_cache, kv.block_table[b:b + 1],
-                                      kv.context_lens[b:b + 1], SCALE)
-        assert np.abs(o[b:b + 1] - ref).max() <= ATOL_F32, b
+    o = out.cpu().numpy().astype(np.float64)
+    ob = bf16_bits(outb)
+    del kc, vc
+
+    def reference(b):
+        return oracle.decode_attention(q[b:b + 1], kv.k_cache, kv.v_cache, kv.block_table[b:b + 1],
+                                       kv.context_lens[b:b + 1], SCALE)
+
+    with concurrent.futures.ThreadPoolExecutor(_host_threads()) as ex:
+        ref = np.concatenate(list(ex.map(reference, range(B))))
+    err = np.abs(o - ref).max(axis=(1, 2))
+    assert (err <= ATOL_F32).all(), np.argwhere(err > ATOL_F32).ravel()
+    assert_bf16_close(ob, oracle.round_bf16(ref), "out_bf16")
+    print(f"ragged B=64: worst |out - oracle| = {err.max():.2e} over {B} sequences")
 
 
 def test_long_split_kv_t131072_np256():

@@ -142,6 +142,20 @@ def test_multi_refuses_too_many_columns_and_flags_short_contexts():
     assert np.isfinite(of).all()
 
 
+def test_multi_short_context_with_the_separate_merge_kernel():
+    """T < M with more than 64 partitions (the merge runs as its own kernel):
+    the short sequence still gets zeros and the flag, the other its
+    attention."""
+    kv = inputs.paged_kv(912, [2, 2240], Hkv=8, page_size=16, fill_unused="normal")
+    assert pg.decode_attn_partition_count(2, 8, 16, kv.max_pages, 70) > 64
+    q = _queries(913, 2, 3, 16)
+    of, _ = run_multi_attention(kv, q, num_partitions=70)
+    assert pg.device_error_flags() & binding.DEVERR_BAD_CONTEXT
+    assert np.all(of[0] == 0)
+    ref = oracle.decode_attention_multi(q[1:], kv.k_cache, kv.v_cache, kv.block_table[1:], kv.context_lens[1:], SCALE)
+    assert np.abs(of[1:] - ref).max() <= ATOL_F32
+
+
 def test_multi_token_workload_layers_full_size():
     """Two layers of the multi-token verification workload (T = 8192, M = 4)
     at full size, prologue then attention, against the oracle's chain."""

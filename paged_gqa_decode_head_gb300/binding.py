@@ -72,13 +72,14 @@ def library_path() -> str:
     return os.path.join(_HERE, _LIB_NAME)
 
 
-def load_library():
-    """Load libpgqa.so (built by __graft_entry__.build()); raise if missing."""
+def load_library(path: str | None = None):
+    """Load libpgqa.so (built by __graft_entry__.build()), or the library at
+    `path` (the timeline build) on the first call; raise if missing."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = library_path()
+        path = path or library_path()
         if not os.path.exists(path):
             raise PgqaError("load_library", -5, f"{path} is missing: build it with __graft_entry__.build()")
         lib = ctypes.CDLL(path)

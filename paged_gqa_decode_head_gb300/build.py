@@ -18,6 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpgqa.so")
+# the same library with the split kernel's per-phase %globaltimer stamps
+# compiled in (see timeline.py); never built by default
+BUILD_TIMELINE = os.path.join(HERE, "_build_timeline")
+LIB_TIMELINE = os.path.join(HERE, "libpgqa_timeline.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -28,10 +32,12 @@ def nvcc() -> str:
     return exe
 
 
-def _flags(verbose_ptxas: bool) -> list[str]:
+def _flags(verbose_ptxas: bool, timeline: bool = False) -> list[str]:
     f = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *ARCH]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
+    if timeline:
+        f += ["-DPGQA_TIMELINE"]
     return f
 
 
@@ -45,35 +51,38 @@ def _deps() -> list[str]:
     return files
 
 
-def _compile(src: str, verbose_ptxas: bool) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *_flags(verbose_ptxas), "-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, timeline: bool = False) -> tuple[str, str]:
+    obj = os.path.join(BUILD_TIMELINE if timeline else BUILD, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *_flags(verbose_ptxas, timeline), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link libpgqa.so; returns its path. Skips work when up to date."""
-    if not force and not verbose_ptxas and os.path.exists(LIB):
+def build(force: bool = False, verbose_ptxas: bool = False, timeline: bool = False) -> str:
+    """Compile and link libpgqa.so (timeline=True: libpgqa_timeline.so, the
+    same sources with the per-phase stamps); returns its path. Skips work
+    when up to date."""
+    lib = LIB_TIMELINE if timeline else LIB
+    if not force and not verbose_ptxas and os.path.exists(lib):
         newest = max(os.path.getmtime(p) for p in _deps())
-        if os.path.getmtime(LIB) >= newest:
-            return LIB
-    os.makedirs(BUILD, exist_ok=True)
+        if os.path.getmtime(lib) >= newest:
+            return lib
+    os.makedirs(BUILD_TIMELINE if timeline else BUILD, exist_ok=True)
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+        results = list(ex.map(lambda s: _compile(s, verbose_ptxas, timeline), srcs))
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -59,6 +59,41 @@ __device__ unsigned g_flags_decode;
 
 __device__ __forceinline__ void raise_flag(unsigned f) { atomicOr(&g_flags_decode, f); }
 
+// Timeline builds (-DPGQA_TIMELINE, a separate library made by the package's
+// timeline module) stamp %globaltimer at each phase of the split kernel into
+// a caller buffer [launch][CTA][kTimelineSlots]; other builds compile the
+// stamps out. Slots: 0 CTA start, 1 block-table entries in hand, 2 first
+// requests issued, 3 grid dependency released, 4 query rotated (fused step),
+// 5 a warp's second chunk landed, 6 last chunk landed (latest warp), 7 warp
+// records merged, 8 partition state written, 9 ticket back, 10 merge done.
+constexpr int kTimelineSlots = 12;
+#ifdef PGQA_TIMELINE
+unsigned long long *g_timeline_buf = nullptr; // host copy of the attached buffer
+int g_timeline_launches = 1, g_timeline_next = 0;
+#define TL_INDEX(slot)                                                                                       \
+    ((static_cast<size_t>(p.tl_launch) * gridDim.x * gridDim.y * gridDim.z + blockIdx.x +                     \
+      gridDim.x * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z)) *                                \
+         kTimelineSlots +                                                                                     \
+     (slot))
+#define TL_STAMP(slot)                                                                                       \
+    do {                                                                                                     \
+        if (p.tl && threadIdx.x == 0)                                                                        \
+            p.tl[TL_INDEX(slot)] = globaltimer_ns();                                                         \
+    } while (0)
+#define TL_STAMP_LATEST(slot)                                                                                \
+    do {                                                                                                     \
+        if (p.tl && (threadIdx.x & 31) == 0)                                                                 \
+            atomicMax(&p.tl[TL_INDEX(slot)], globaltimer_ns());                                              \
+    } while (0)
+#else
+#define TL_STAMP(slot) \
+    do {               \
+    } while (0)
+#define TL_STAMP_LATEST(slot) \
+    do {                      \
+    } while (0)
+#endif
+
 constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
@@ -124,6 +159,10 @@ struct SplitParams {
     uint16_t *k_cache, *v_cache, *q_out;
     float eps;
     RopeFreqs freqs;
+#ifdef PGQA_TIMELINE
+    unsigned long long *tl; // timeline buffer, or NULL
+    int tl_launch;          // this launch's index in it
+#endif
 };
 
 // Row (of the [B][M][Hq] query / output arrays) of column n of KV head kvh;
@@ -371,6 +410,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     const int b = blockIdx.z;
 
     allow_dependent_launch();
+    TL_STAMP(0);
     unsigned char *stages = smem + warp * kStages * kStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOffset) + warp * kStages;
     if (lane == 0) {
@@ -457,6 +497,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
 #pragma unroll
     for (int k = 0; k < kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
+    TL_STAMP(1);
     // Only the first kPrewait chunks of each warp are requested before
     // griddepcontrol.wait: in the fused step the rest would queue in the
     // memory system ahead of the previous layer's merge and this layer's
@@ -467,6 +508,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
             if (k < first && k < kPrewait && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
+    TL_STAMP(2);
 
     // fused step: what the prologue needs that no earlier kernel writes
     // (gains, rotation, the append slot) is prepared before the wait.
@@ -514,6 +556,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
         load_head(p.gamma_k, gain_k);
 
     grid_dependency_wait();
+    TL_STAMP(3);
 
     // The new tokens' q, k, v come from the previous kernels: load them now,
     // ahead of the remaining bulk requests.
@@ -585,6 +628,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
             __syncwarp();
         }
         st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
+        TL_STAMP(4);
         if (!kMulti && appends) {
             // single token: off the other warps' path; the row waits in
             // shared memory for the patch of its staged chunk
@@ -643,6 +687,10 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
                 const bool landed = mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1);
                 if (!__all_sync(0xFFFFFFFFu, landed))
                     ok = false;
+                if (k == 1)
+                    TL_STAMP(5);
+                if (k == my_chunks - 1)
+                    TL_STAMP_LATEST(6);
                 rows[c] = stage_rows[k % kStages];
                 if (kFused && k == new_chunk && rows[c] > 0) {
                     // the staged copy predates the append: put the new row in
@@ -727,6 +775,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     // Every copy into this warp's stages has landed: they can hold its record.
     st.store_record(reinterpret_cast<float *>(stages));
     __syncthreads();
+    TL_STAMP(7);
 
     for (int e = threadIdx.x; e < NCOL * kHeadDim; e += kWarps * 32) {
         const int h = e / kHeadDim;
@@ -764,6 +813,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     if (n_parts == 1 || !p.fused_merge)
         return;
 
+    TL_STAMP(8);
     // Ticket: the CTA that finishes last for this (sequence, KV head) merges.
     // The barrier orders every thread's partial-state stores before thread
     // 0's release; its acquire (when last) orders the other CTAs' stores
@@ -775,10 +825,15 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     if (threadIdx.x == 0)
         *ticket_slot = atomic_add_acq_rel_gpu(ticket, 1u);
     __syncthreads();
+    TL_STAMP(9);
     if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
         return;
     merge_in_last_cta<NCOL, kMulti, S::kThreads>(p, b, kvh, n_parts, smem,
                                                  reinterpret_cast<uint64_t *>(smem + kMergeBarOffset));
+#ifdef PGQA_TIMELINE
+    __syncthreads();
+    TL_STAMP(10);
+#endif
     if (threadIdx.x == 0)
         *ticket = 0u; // ready for the next call
 }
@@ -1084,6 +1139,11 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
+#ifdef PGQA_TIMELINE
+    kp.tl = g_timeline_buf;
+    kp.tl_launch = g_timeline_next;
+    g_timeline_next = (g_timeline_next + 1) % g_timeline_launches;
+#endif
     const bool pair = use_pair_shape(NCOL, M, a.B, a.Hkv, a.num_partitions, a.pages_per_part * a.page_size,
                                      a.sm_count);
     const long merge_bytes = static_cast<long>(NCOL) * a.num_partitions * kHeadDim * 4 +
@@ -1193,6 +1253,19 @@ cudaError_t launch_wait_selftest(cudaStream_t stream)
     wait_selftest_kernel<<<1, 32, 0, stream>>>();
     return cudaGetLastError();
 }
+
+#ifdef PGQA_TIMELINE
+// Attach (or, with NULL, detach) the timeline buffer: `launches` slots of
+// [CTAs][kTimelineSlots] u64, filled in turn by the following split-kernel
+// launches (captured graphs keep the slot they were captured with).
+extern "C" int pgqa_timeline_attach(unsigned long long *buf, int launches)
+{
+    g_timeline_buf = buf;
+    g_timeline_launches = launches > 0 ? launches : 1;
+    g_timeline_next = 0;
+    return kTimelineSlots;
+}
+#endif
 
 cudaError_t read_flags_decode(unsigned *flags, bool clear)
 {

@@ -18,10 +18,21 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpgqa.so")
-# the same library with the split kernel's per-phase %globaltimer stamps
-# compiled in (see timeline.py); never built by default
-BUILD_TIMELINE = os.path.join(HERE, "_build_timeline")
-LIB_TIMELINE = os.path.join(HERE, "libpgqa_timeline.so")
+# Measurement builds of the same sources, never built by default:
+# "timeline" compiles in the split kernel's per-phase %globaltimer stamps
+# (see timeline.py); "core_fold" folds single-token chunks on CUDA cores
+# instead of tensor cores, to measure the MMA fold against it.
+VARIANTS = {
+    "timeline": ("-DPGQA_TIMELINE", "libpgqa_timeline.so"),
+    "core_fold": ("-DPGQA_CORE_FOLD", "libpgqa_corefold.so"),
+}
+
+
+def _variant_paths(variant):
+    if variant is None:
+        return BUILD, LIB
+    define, name = VARIANTS[variant]
+    return os.path.join(HERE, "_build_" + variant), os.path.join(HERE, name)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,12 +43,12 @@ def nvcc() -> str:
     return exe
 
 
-def _flags(verbose_ptxas: bool, timeline: bool = False) -> list[str]:
+def _flags(verbose_ptxas: bool, variant=None) -> list[str]:
     f = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC, *ARCH]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
-    if timeline:
-        f += ["-DPGQA_TIMELINE"]
+    if variant is not None:
+        f += [VARIANTS[variant][0]]
     return f
 
 
@@ -51,28 +62,27 @@ def _deps() -> list[str]:
     return files
 
 
-def _compile(src: str, verbose_ptxas: bool, timeline: bool = False) -> tuple[str, str]:
-    obj = os.path.join(BUILD_TIMELINE if timeline else BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *_flags(verbose_ptxas, timeline), "-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, variant=None) -> tuple[str, str]:
+    obj = os.path.join(_variant_paths(variant)[0], os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *_flags(verbose_ptxas, variant), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, timeline: bool = False) -> str:
-    """Compile and link libpgqa.so (timeline=True: libpgqa_timeline.so, the
-    same sources with the per-phase stamps); returns its path. Skips work
-    when up to date."""
-    lib = LIB_TIMELINE if timeline else LIB
+def build(force: bool = False, verbose_ptxas: bool = False, variant: str | None = None) -> str:
+    """Compile and link libpgqa.so (or a measurement build named in
+    VARIANTS); returns its path. Skips work when up to date."""
+    build_dir, lib = _variant_paths(variant)
     if not force and not verbose_ptxas and os.path.exists(lib):
         newest = max(os.path.getmtime(p) for p in _deps())
         if os.path.getmtime(lib) >= newest:
             return lib
-    os.makedirs(BUILD_TIMELINE if timeline else BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose_ptxas, timeline), srcs))
+        results = list(ex.map(lambda s: _compile(s, verbose_ptxas, variant), srcs))
     if verbose_ptxas:
         for _, log in results:
             sys.stderr.write(log)

@@ -75,7 +75,7 @@ def main(argv=None):
     from . import binding, build, inputs
     from .runner import DecodeStep
 
-    path = args.library or build.build(timeline=True)
+    path = args.library or build.build(variant="timeline")
     lib = binding.load_library(path)
     lib.pgqa_timeline_attach.argtypes = [ctypes.c_void_p, ctypes.c_int]
     lib.pgqa_timeline_attach.restype = ctypes.c_int

@@ -57,12 +57,6 @@ def parse_args():
                          "measured on their own (one JSON line per variant, not the headline line)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default 28); a smaller count is only for profiling captures")
-    ap.add_argument("--fold-ab", action="store_true",
-                    help="same-process A/B of the tensor-core fold against the CUDA-core fold build "
-                         "(the 28-layer T=8192 chain, g=2, and the T=131072 Hq=32 context, g=4)")
-    ap.add_argument("--fold-ab-only", choices=["mma", "core"], default=None,
-                    help="with --fold-ab: load only one of the two builds (for profiling captures)")
-    ap.add_argument("--fold-ab-case", choices=["all", "chain", "long"], default="all")
     return ap.parse_args()
 
 
@@ -806,133 +800,8 @@ def run_secondary(args):
     sampler.stop()
 
 
-def run_fold_ab(args):
-    """The tensor-core fold (mma.sync, the product build) against the same
-    kernel folding on CUDA cores (the core_fold build: same TMA ring,
-    partitions, merge and launches), both loaded in this process, graphs
-    captured over the same buffers and timed in alternation."""
-    import numpy as np
-    import torch
-
-    import oracle
-    from paged_gqa_decode_head_gb300 import binding, build, inputs
-    from paged_gqa_decode_head_gb300.runner import DecodeStep, to_device_bf16, to_device_i32
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    idle = gpu_idle_check(smi_gpu_id(dev))
-    names = [n for n in ("mma", "core") if args.fold_ab_only in (None, n)]
-    libs = {}
-    for name in names:
-        path = build.build(variant=None if name == "mma" else "core_fold")
-        binding._lib = None
-        libs[name] = binding.load_library(path)
-    keep = []
-    graphs = {}  # (case, name) -> (graph, launches per replay)
-    outs = {}
-    L = args.layers or 28
-    scale = 1.0 / math.sqrt(128)
-
-    def capture(fn):
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream(dev).wait_stream(side)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fn()
-        return g
-
-    if args.fold_ab_case in ("all", "chain"):
-        w = inputs.WORKLOADS[WORKLOAD]
-        step = DecodeStep(inputs.qwen3_layers(layers=L), Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"])
-        for name in names:
-            binding._lib = libs[name]
-            graphs[("chain fused step (g=2)", name)] = (step.capture(prologue=True, fused=True), L)
-            graphs[("chain attention alone (g=2)", name)] = (step.capture(prologue=False), L)
-            step.run(prologue=True, fused=True)
-            torch.cuda.synchronize()
-            outs[("chain", name)] = step.outputs.clone()
-        keep.append(step)
-    if args.fold_ab_case in ("all", "long"):
-        kv, q = inputs.long_split_kv()
-        wl = inputs.WORKLOADS["long_split_kv_t128k"]
-        B, Hq, Hkv = 1, wl["Hq"], wl["Hkv"]
-        bufs = dict(q=to_device_bf16(q, dev), kc=to_device_bf16(kv.k_cache, dev), vc=to_device_bf16(kv.v_cache, dev),
-                    bt=to_device_i32(kv.block_table, dev), ctx=to_device_i32(kv.context_lens, dev),
-                    out=torch.empty((B, Hq, 128), dtype=torch.float32, device=dev))
-        keep.append(bufs)
-        for npr, label in ((0, "automatic NP"), (wl["T"] // wl["partition"], "512-position partitions")):
-            n = binding.decode_attn_workspace_size(B, Hq, Hkv, 128, kv.page_size, kv.max_pages, npr)
-            ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)
-            keep.append(ws)
-            reps = min(L, 8)
-            for name in names:
-                binding._lib = libs[name]
-
-                def launches(npr=npr, ws=ws):
-                    for _ in range(reps):
-                        binding.decode_attn_paged(bufs["q"], bufs["kc"], bufs["vc"], bufs["bt"], bufs["ctx"], scale,
-                                                  out_f32=bufs["out"], workspace=ws, num_partitions=npr)
-
-                graphs[(f"T=131072 Hq=32 ({label}, g=4)", name)] = (capture(launches), reps)
-                launches()
-                torch.cuda.synchronize()
-                outs[(f"long {label}", name)] = bufs["out"].clone()
-        ref = oracle.decode_attention(q, kv.k_cache, kv.v_cache, kv.block_table, kv.context_lens, scale)
-        for (case, name), o in list(outs.items()):
-            if case.startswith("long"):
-                outs[(case + " vs oracle", name)] = float(np.abs(o.cpu().numpy() - ref).max())
-
-    sampler = ClockSampler(smi_gpu_id(dev))
-    sampler.start()
-    time.sleep(0.5)
-    times = {k: [] for k in graphs}
-    rounds = max(3, min(args.steps, 20))
-    t0 = time.time()
-    for _ in range(rounds):
-        for key, (g, per) in graphs.items():
-            for _ in range(3):
-                g.replay()
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(20):
-                g.replay()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            times[key].append(e0.elapsed_time(e1) * 1e3 / (20 * per))
-    t1 = time.time()
-    sampler.stop()
-    clocks = sampler.summary(t0, t1)
-    cases = sorted({c for c, _ in graphs}, key=lambda c: list(graphs).index((c, names[0])))
-    for case in cases:
-        line = {"metric": f"fold A/B: {case}", "unit": "us per launch (median of rounds)", "clocks": clocks,
-                "gpu_idle_at_start": idle}
-        for name in names:
-            line[name] = statistics.median(times[(case, name)])
-        if len(names) == 2:
-            line["mma_speedup"] = line["core"] / line["mma"]
-        print(json.dumps(line), flush=True)
-    diffs = {}
-    for (case, name), o in outs.items():
-        if isinstance(o, float):
-            diffs[f"{case} ({name})"] = o
-    if len(names) == 2:
-        for (case, name), o in outs.items():
-            if name == "mma" and not isinstance(o, float):
-                diffs[f"{case}: max |core - mma|"] = float((outs[(case, "core")] - o).abs().max())
-    print(json.dumps({"fold A/B outputs": diffs}), flush=True)
-    assert binding.device_error_flags() == 0
-
-
 def main():
     args = parse_args()
-    if args.fold_ab:
-        run_fold_ab(args)
-        return
     rank, world, local = dist_env()
     if args.gpus != world and world != 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)

@@ -20,11 +20,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpgqa.so")
 # Measurement builds of the same sources, never built by default:
 # "timeline" compiles in the split kernel's per-phase %globaltimer stamps
-# (see timeline.py); "core_fold" folds single-token chunks on CUDA cores
-# instead of tensor cores, to measure the MMA fold against it.
+# (see timeline.py).
 VARIANTS = {
     "timeline": ("-DPGQA_TIMELINE", "libpgqa_timeline.so"),
-    "core_fold": ("-DPGQA_CORE_FOLD", "libpgqa_corefold.so"),
 }
 
 

@@ -43,7 +43,6 @@
 #include <algorithm>
 #include <cmath>
 #include <mutex>
-#include <type_traits>
 
 #include <cuda.h>
 
@@ -95,15 +94,6 @@ int g_timeline_launches = 1, g_timeline_next = 0;
     } while (0)
 #endif
 
-// Builds with -DPGQA_CORE_FOLD fold the single-token chunks on CUDA cores
-// (CoreWarp) instead of tensor cores (MmaWarp): the same ring, partitions,
-// merge and launch, to measure what the MMA fold itself is worth.
-#ifdef PGQA_CORE_FOLD
-constexpr bool kCoreFold = true;
-#else
-constexpr bool kCoreFold = false;
-#endif
-
 constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
@@ -124,9 +114,7 @@ template <int kW, int kS, int kCtas> struct Shape {
     static constexpr int kMergeBarOffset = kTicketOffset + 8;
     static constexpr int kQBufOffset = (kMergeBarOffset + 8 + 15) & ~15;
     static constexpr int kPatchOffset = kQBufOffset + kMaxGroup * kHeadDim * 2;
-    static constexpr int kQf32Offset = kPatchOffset + 4 * kHeadDim; // CUDA-core fold's fp32 query
-    static constexpr int kSmem =
-        1024 /* alignment slack */ + kQf32Offset + (kCoreFold ? kMaxGroup * kHeadDim * 4 : 0);
+    static constexpr int kSmem = 1024 /* alignment slack */ + kPatchOffset + 4 * kHeadDim;
     // The in-kernel merge copies the G x n partition accumulators of its
     // group into the stage area, followed by its scratch (weights, sums, a
     // float4 per thread); launch_decode falls back to merge_kernel when they
@@ -382,129 +370,6 @@ template <int NCOL> struct MmaWarp {
     }
 };
 
-#ifdef PGQA_CORE_FOLD
-// The same per-warp online-softmax state as MmaWarp, folded on CUDA cores:
-// lanes 2j and 2j+1 hold key j's two half dot products with every query
-// column (the query, rounded to bf16, as fp32 in shared memory), lane L owns
-// output dims 4L..4L+3 of every column; p_j reaches the PV lanes by shuffle.
-template <int NCOL> struct CoreWarp {
-    uint32_t qs;         // shared address of the fp32 query [NCOL][128]
-    float acc[NCOL][4];  // O, dims 4 * lane .. + 3
-    float m[NCOL];       // running max (base-2 units), the same in every lane
-    float l[NCOL];       // sum of p over this lane's keys (even lanes)
-
-    __device__ __forceinline__ void init(const float *q_f32)
-    {
-        qs = smem_addr(q_f32);
-        clear();
-    }
-
-    __device__ __forceinline__ void clear()
-    {
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c) {
-            m[c] = kEmptyMax;
-            l[c] = 0.f;
-            acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
-        }
-    }
-
-    __device__ __forceinline__ void fold_one(uint32_t stage, int rows, float scale_log2)
-    {
-        const int lane = threadIdx.x & 31, j = lane >> 1, h = lane & 1;
-        float s[NCOL];
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c)
-            s[c] = 0.f;
-#pragma unroll 2
-        for (int u = 0; u < 8; ++u) {
-            float kf[8];
-            unpack8(lds128(stage + h * kBoxBytes + j * 128 + ((u ^ (j & 7)) << 4)), kf);
-#pragma unroll
-            for (int c = 0; c < NCOL; ++c) {
-                const uint32_t qa = qs + (c * kHeadDim + 64 * h + 8 * u) * 4;
-                const uint4 q0 = lds128(qa), q1 = lds128(qa + 16);
-                s[c] = fmaf(kf[0], __uint_as_float(q0.x), s[c]);
-                s[c] = fmaf(kf[1], __uint_as_float(q0.y), s[c]);
-                s[c] = fmaf(kf[2], __uint_as_float(q0.z), s[c]);
-                s[c] = fmaf(kf[3], __uint_as_float(q0.w), s[c]);
-                s[c] = fmaf(kf[4], __uint_as_float(q1.x), s[c]);
-                s[c] = fmaf(kf[5], __uint_as_float(q1.y), s[c]);
-                s[c] = fmaf(kf[6], __uint_as_float(q1.z), s[c]);
-                s[c] = fmaf(kf[7], __uint_as_float(q1.w), s[c]);
-            }
-        }
-        float pr[NCOL];
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c) {
-            float sc = (s[c] + __shfl_xor_sync(0xFFFFFFFFu, s[c], 1)) * scale_log2;
-            if (j >= rows)
-                sc = -INFINITY;
-            float cm = sc;
-#pragma unroll
-            for (int off = 2; off < 32; off <<= 1)
-                cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
-            const float mn = fmaxf(m[c], cm);
-            if (mn > m[c]) {
-                const float corr = exp2f(m[c] - mn);
-                l[c] *= corr;
-                acc[c][0] *= corr, acc[c][1] *= corr, acc[c][2] *= corr, acc[c][3] *= corr;
-                m[c] = mn;
-            }
-            pr[c] = exp2f(sc - m[c]); // masked: exp2(-inf) = 0
-            if (h == 0)
-                l[c] += pr[c];
-        }
-        const int x = (4 * lane) & 63, uu = x >> 3;
-        const uint32_t vbase = stage + (2 + (lane >> 4)) * kBoxBytes + (x & 7) * 2;
-#pragma unroll 4
-        for (int jj = 0; jj < kChunkTokens; ++jj) {
-            uint32_t v01, v23;
-            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                         : "=r"(v01), "=r"(v23)
-                         : "r"(vbase + jj * 128 + ((uu ^ (jj & 7)) << 4)));
-            const float v0 = bf16_lo(v01), v1 = bf16_hi(v01), v2 = bf16_lo(v23), v3 = bf16_hi(v23);
-#pragma unroll
-            for (int c = 0; c < NCOL; ++c) {
-                const float pj = __shfl_sync(0xFFFFFFFFu, pr[c], 2 * jj);
-                acc[c][0] = fmaf(pj, v0, acc[c][0]);
-                acc[c][1] = fmaf(pj, v1, acc[c][1]);
-                acc[c][2] = fmaf(pj, v2, acc[c][2]);
-                acc[c][3] = fmaf(pj, v3, acc[c][3]);
-            }
-        }
-    }
-
-    template <int NC, bool kPerColumn, int N>
-    __device__ __forceinline__ void fold(const uint32_t (&stage)[N], const int (&lim0)[N], const int (&)[N],
-                                         float scale_log2)
-    {
-        static_assert(!kPerColumn, "single-token columns only");
-#pragma unroll 1
-        for (int c = 0; c < NC; ++c)
-            fold_one(stage[c], lim0[c], scale_log2);
-    }
-
-    // [NCOL][128] O, then [NCOL] m, then [NCOL] l (the MmaWarp record layout)
-    __device__ __forceinline__ void store_record(float *rec)
-    {
-        const int lane = threadIdx.x & 31;
-#pragma unroll
-        for (int c = 0; c < NCOL; ++c) {
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1)
-                l[c] += __shfl_xor_sync(0xFFFFFFFFu, l[c], off);
-            *reinterpret_cast<float4 *>(rec + c * kHeadDim + 4 * lane) =
-                make_float4(acc[c][0], acc[c][1], acc[c][2], acc[c][3]);
-            if (lane == 0) {
-                rec[NCOL * kHeadDim + c] = m[c];
-                rec[NCOL * kHeadDim + NCOL + c] = l[c];
-            }
-        }
-    }
-};
-#endif
-
 // The last CTA of a (sequence, KV head) to finish merges the n (2..64)
 // partition states of its columns (partition_merge.cuh).
 template <int NCOL, bool kMulti, int kThreads>
@@ -699,14 +564,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     const size_t krow = ((static_cast<size_t>(b) * (kMulti ? p.M : 1) + (kMulti ? warp : 0)) * p.Hkv + kvh) * kHeadDim;
     float xq[4], xk[4];
     uint16_t new_v[4] = {0, 0, 0, 0};
-#ifdef PGQA_CORE_FOLD
-    constexpr bool kCore = !kMulti;
-    using FoldWarp = std::conditional_t<kCore, CoreWarp<NCOL>, MmaWarp<NCOL>>;
-    float *q_f32 = reinterpret_cast<float *>(smem + S::kQf32Offset);
-#else
-    using FoldWarp = MmaWarp<NCOL>;
-#endif
-    FoldWarp st;
+    MmaWarp<NCOL> st;
     const int col = lane >> 2; // this lane's B-operand column
     if (has_q)
         load_head(p.q_raw + qrow, xq);
@@ -716,17 +574,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
         for (int i = 0; i < 4; ++i)
             new_v[i] = p.v_new[krow + lane + 32 * i];
     }
-#ifdef PGQA_CORE_FOLD
-    if constexpr (!kFused && kCore) {
-        for (int e = threadIdx.x; e < NCOL * kHeadDim; e += kWarps * 32)
-            q_f32[e] = __uint_as_float(static_cast<uint32_t>(
-                           p.q[column_row<kMulti>(p, b, kvh, e / kHeadDim) * kHeadDim + e % kHeadDim])
-                       << 16);
-        __syncthreads();
-        st.init(q_f32);
-    } else
-#endif
-        if constexpr (!kFused)
+    if constexpr (!kFused)
         st.init(col < NCOL ? p.q + column_row<kMulti>(p, b, kvh, col) * kHeadDim : nullptr);
     // the fused multi-token step requests new-token chunks after the appends
     constexpr bool kDeferNew = kFused && kMulti;
@@ -748,9 +596,6 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
             for (int i = 0; i < 4; ++i) {
                 const uint16_t bits = f32_to_bf16_bits(xq[i]);
                 q_buf[warp * kHeadDim + lane + 32 * i] = bits;
-#ifdef PGQA_CORE_FOLD
-                q_f32[warp * kHeadDim + lane + 32 * i] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-#endif
                 if (part == 0 && p.q_out)
                     p.q_out[qrow + lane + 32 * i] = bits;
             }
@@ -782,12 +627,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
             }
             __syncwarp();
         }
-#ifdef PGQA_CORE_FOLD
-        if constexpr (kCore)
-            st.init(q_f32);
-        else
-#endif
-            st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
+        st.init(col < NCOL ? q_buf + col * kHeadDim : nullptr);
         TL_STAMP(4);
         if (!kMulti && appends) {
             // single token: off the other warps' path; the row waits in

@@ -55,6 +55,8 @@ def parse_args():
                              "qwen3_0p6b_t8k_m4", "qwen3_0p6b_t8k_int8"],
                     help="the headline step (default) or one of the larger parity workloads, "
                          "measured on their own (one JSON line per variant, not the headline line)")
+    ap.add_argument("--ragged-batch", type=int, default=None,
+                    help="with --workload ragged_b64: only the first N sequences (a smaller case for captures)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers per step (default 28); a smaller count is only for profiling captures")
     return ap.parse_args()
@@ -464,6 +466,34 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def host_tiled_overlap(trace, group_bytes: int) -> dict:
+    """Summary of a traced host-tiled run: per copy group g the events
+    [4g] copy start, [4g+1] copy end, [4g+2] update start, [4g+3] update end.
+    Returns the run's span, the time the copy stream and the compute stream
+    were busy, how much of the update time ran while a copy was in flight,
+    and the link rate of the copies themselves."""
+    t = [trace[0].elapsed_time(ev) * 1e3 for ev in trace]  # us after the first copy start
+    G = len(t) // 4
+    copies = [(t[4 * g], t[4 * g + 1]) for g in range(G)]
+    updates = [(t[4 * g + 2], t[4 * g + 3]) for g in range(G)]
+    span = max(e for _, e in updates) - copies[0][0]
+
+    def overlap(a, b):
+        return max(0.0, min(a[1], b[1]) - max(a[0], b[0]))
+
+    copy_busy = sum(e - s_ for s_, e in copies)
+    update_busy = sum(e - s_ for s_, e in updates)
+    update_under_copy = sum(overlap(u, c) for u in updates for c in copies)
+    waits = [updates[g][0] - copies[g][1] for g in range(G)]
+    return {"groups": G, "span_us": span, "copy_busy_us": copy_busy, "update_busy_us": update_busy,
+            "copy_busy_frac": copy_busy / span, "update_under_copy_frac": update_under_copy / max(update_busy, 1e-9),
+            "copy_gbs": G * group_bytes / (copy_busy * 1e-6) / 1e9,
+            "median_copy_us": statistics.median(e - s_ for s_, e in copies),
+            "median_update_us": statistics.median(e - s_ for s_, e in updates),
+            "median_copy_end_to_update_start_us": statistics.median(waits),
+            "first_groups_us": [[round(x, 1) for x in (c[0], c[1], u[0], u[1])] for c, u in zip(copies[:4], updates[:4])]}
+
+
 def run_secondary(args):
     """Bandwidth of one of the larger workloads: KV bytes per second of
     decode_attn_paged (ragged batch, long split-KV context), or bytes per second
@@ -529,7 +559,7 @@ def run_secondary(args):
 
     if args.workload in ("ragged_b64", "long_split_kv_t128k"):
         if args.workload == "ragged_b64":
-            kv, q = inputs.ragged_b64()
+            kv, q = inputs.ragged_b64(args.ragged_batch)
             nps = [0]
             jobs = [lambda b=b: oracle.decode_attention(q[b:b + 1], kv.k_cache, kv.v_cache, kv.block_table[b:b + 1],
                                                         kv.context_lens[b:b + 1], scale)
@@ -791,6 +821,16 @@ def run_secondary(args):
                                                  copy_stream=copy_stream))
         emit(f"attn_host_tiled_run ({tile}-position tiles, {per_copy} per copy, {n_slots} slots)", nbytes, s, link,
              "GB/s", "measured link", {"config": cfg})
+        # one more run with an event pair around every copy and every group
+        # of updates (attn_host_tiled_run_traced): how the copies and the
+        # updates overlap
+        n_groups = -(-T // (tile * per_copy))
+        trace = [torch.cuda.Event(enable_timing=True) for _ in range(4 * n_groups)]
+        pg.attn_host_tiled_run(qd, hk, hv, scale, slots_k, slots_v, events, m, l, acc, out_f32=out, tile_len=tile,
+                               tiles_per_copy=per_copy, copy_stream=copy_stream, trace_events=trace)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"metric": f"{args.workload} attn_host_tiled_run pipeline trace ({per_copy} per copy)",
+                          **host_tiled_overlap(trace, per_copy * tile * Hkv * 128 * 2 * 2 * B)}), flush=True)
         del slots_k, slots_v
     n = pg.attn_host_direct_workspace_size(B, Hq, Hkv, T, 0)
     ws = torch.zeros(max(16, n), dtype=torch.uint8, device=dev)

@@ -392,6 +392,31 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
                         cudaStream_t copy_stream);
 
 /*
+ * attn_host_tiled_run_traced -- attn_host_tiled_run that also records
+ * caller-created events around every copy and every group of tile updates,
+ * so that the overlap of copies and updates can be measured ("EdgeTransformer
+ * Engine", KV-offload design and its current-limits list: the overlap there
+ * was inferred, not measured). Same arguments and results, plus:
+ *   trace_events    4 * n_trace_groups events created by the caller with
+ *                   timing enabled; for copy group g < n_trace_groups (the
+ *                   g-th copy of tiles_per_copy tiles):
+ *                     [4g]     before the group's K copy   (copy_stream)
+ *                     [4g + 1] after its V copy            (copy_stream)
+ *                     [4g + 2] before its first tile update (compute_stream,
+ *                              after the wait for the copy)
+ *                     [4g + 3] after its last tile update  (compute_stream)
+ *                   Groups past n_trace_groups are not traced.
+ * PGQA_ERR_INVALID_ARG for a NULL event or a negative count. Nothing is
+ * allocated.
+ */
+int attn_host_tiled_run_traced(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v, int T,
+                               int B, int Hq, int Hkv, int D, float scale, int tile_len, int tiles_per_copy,
+                               int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
+                               cudaEvent_t const *events, float *m, float *l, float *acc, float *out_f32,
+                               pgqa_bf16 *out_bf16, cudaStream_t compute_stream, cudaStream_t copy_stream,
+                               cudaEvent_t const *trace_events, int n_trace_groups);
+
+/*
  * Zero-copy variant of the host-tiled attention ([EdgeTransformerEngine],
  * KV-offload design, whose state (m, l, acc) and exact merge it keeps): the
  * history stays in pinned host memory and the kernel reads it over the host

@@ -42,6 +42,7 @@ EXPORTED = (
     "attn_tile_update",
     "attn_tile_finalize",
     "attn_host_tiled_run",
+    "attn_host_tiled_run_traced",
     "attn_host_direct_partition_count",
     "attn_host_direct_workspace_size",
     "attn_host_direct",
@@ -124,6 +125,9 @@ def load_library(path: str | None = None):
         lib.attn_tile_finalize.restype = I
         lib.attn_host_tiled_run.argtypes = [P, P, P, I, I, I, I, I, F, I, I, I, P, P, P, P, P, P, P, P, P, P]
         lib.attn_host_tiled_run.restype = I
+        lib.attn_host_tiled_run_traced.argtypes = [P, P, P, I, I, I, I, I, F, I, I, I, P, P, P, P, P, P, P, P, P, P,
+                                                   P, I]
+        lib.attn_host_tiled_run_traced.restype = I
         lib.attn_host_direct_partition_count.argtypes = [I, I, I, I]
         lib.attn_host_direct_partition_count.restype = I
         lib.attn_host_direct_workspace_size.argtypes = [I, I, I, I, I]
@@ -415,9 +419,11 @@ def attn_tile_finalize(m, l, acc, out_f32=None, out_bf16=None, stream=None) -> N
 
 def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, events, m, l, acc, out_f32=None,
                         out_bf16=None, tile_len: int = 512, tiles_per_copy: int = 1, compute_stream=None,
-                        copy_stream=None) -> None:
+                        copy_stream=None, trace_events=None) -> None:
     """host_k/host_v: pinned CPU bf16 [B, T, Hkv, D]; k_slots/v_slots: lists of device
-    [B, tiles_per_copy * tile_len, Hkv, D] buffers; events: 2*len(k_slots) torch.cuda.Event objects."""
+    [B, tiles_per_copy * tile_len, Hkv, D] buffers; events: 2*len(k_slots) torch.cuda.Event objects.
+    trace_events (optional): 4 * G torch.cuda.Event(enable_timing=True) objects, recorded around
+    the first G copy groups (attn_host_tiled_run_traced)."""
     lib = load_library()
     bf, f32 = torch.bfloat16, torch.float32
     B, Hq, D = q.shape
@@ -433,13 +439,22 @@ def attn_host_tiled_run(q, host_k, host_v, scale: float, k_slots, v_slots, event
     ep = (ctypes.c_void_p * (2 * n))(*[ev.cuda_event for ev in events])
     if copy_stream is None:
         raise ValueError("copy_stream is required (a stream other than the compute stream)")
-    st = lib.attn_host_tiled_run(
-        _dev(q, bf, "q"), _host(host_k, bf, "host_k"), _host(host_v, bf, "host_v"), T, B, Hq, Hkv, D, float(scale),
-        int(tile_len), int(tiles_per_copy), n, ctypes.cast(kp, ctypes.c_void_p), ctypes.cast(vp, ctypes.c_void_p),
-        ctypes.cast(ep, ctypes.c_void_p), _dev(m, f32, "m"), _dev(l, f32, "l"), _dev(acc, f32, "acc"),
-        _dev(out_f32, f32, "out_f32", nullable=True), _dev(out_bf16, bf, "out_bf16", nullable=True),
-        _stream(compute_stream), _stream(copy_stream))
-    _check("attn_host_tiled_run", st)
+    args = (_dev(q, bf, "q"), _host(host_k, bf, "host_k"), _host(host_v, bf, "host_v"), T, B, Hq, Hkv, D,
+            float(scale), int(tile_len), int(tiles_per_copy), n, ctypes.cast(kp, ctypes.c_void_p),
+            ctypes.cast(vp, ctypes.c_void_p), ctypes.cast(ep, ctypes.c_void_p), _dev(m, f32, "m"),
+            _dev(l, f32, "l"), _dev(acc, f32, "acc"), _dev(out_f32, f32, "out_f32", nullable=True),
+            _dev(out_bf16, bf, "out_bf16", nullable=True), _stream(compute_stream), _stream(copy_stream))
+    if trace_events is None:
+        _check("attn_host_tiled_run", lib.attn_host_tiled_run(*args))
+        return
+    if len(trace_events) % 4:
+        raise ValueError("trace_events: 4 events per traced copy group")
+    for ev in trace_events:
+        if ev.cuda_event == 0:
+            ev.record()  # materialise the lazily created torch event
+    tp = (ctypes.c_void_p * max(1, len(trace_events)))(*[ev.cuda_event for ev in trace_events])
+    _check("attn_host_tiled_run_traced",
+           lib.attn_host_tiled_run_traced(*args, ctypes.cast(tp, ctypes.c_void_p), len(trace_events) // 4))
 
 
 def attn_host_direct_partition_count(B: int, Hkv: int, T: int, num_partitions: int = 0) -> int:

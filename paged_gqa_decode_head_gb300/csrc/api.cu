@@ -506,14 +506,15 @@ int attn_tile_finalize(const float *m, const float *l, const float *acc, int B, 
     return ok();
 }
 
-int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
-                        int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
-                        int tiles_per_copy, int n_slots, pgqa_bf16 *const *k_slots,
-                        pgqa_bf16 *const *v_slots, cudaEvent_t const *events, float *m, float *l,
-                        float *acc, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
-                        cudaStream_t copy_stream)
+// The host-tiled pipeline; trace (n_trace copy groups, 4 events each) may
+// be NULL.
+static int host_tiled_impl(const char *fn, const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
+                           int T, int B, int Hq, int Hkv, int D, float scale, int tile_len, int tiles_per_copy,
+                           int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
+                           cudaEvent_t const *events, float *m, float *l, float *acc, float *out_f32,
+                           pgqa_bf16 *out_bf16, cudaStream_t compute_stream, cudaStream_t copy_stream,
+                           cudaEvent_t const *trace, long n_trace)
 {
-    const char *fn = "attn_host_tiled_run";
     if (int st = check_heads(fn, B, Hq, Hkv, D))
         return st;
     if (T < 0 || tile_len < 1 || tile_len > 512 || n_slots < 2 || n_slots > 8 || tiles_per_copy < 1 ||
@@ -560,6 +561,9 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
         // The slot is free once the updates that last read it have finished.
         if (g >= n_slots && (err = cudaStreamWaitEvent(copy_stream, compute_done[s], 0)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(copy)");
+        const bool traced = trace && g < n_trace;
+        if (traced && (err = cudaEventRecord(trace[4 * g], copy_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: trace event (copy start)");
         // Host rows of sequence b are [b][t0 .. t0+n_span); the slot holds
         // [b][0 .. n_span) packed: a 2-D copy with one row per sequence.
         const size_t row_bytes = static_cast<size_t>(n_span) * pos_bytes;
@@ -580,10 +584,14 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
         }
         if (err != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: tile copy");
+        if (traced && (err = cudaEventRecord(trace[4 * g + 1], copy_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: trace event (copy end)");
         if ((err = cudaEventRecord(copy_done[s], copy_stream)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(copy)");
         if ((err = cudaStreamWaitEvent(compute_stream, copy_done[s], 0)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaStreamWaitEvent(compute)");
+        if (traced && (err = cudaEventRecord(trace[4 * g + 2], compute_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: trace event (update start)");
         for (int p0 = 0; p0 < n_span; p0 += tile_len) {
             const size_t off = static_cast<size_t>(p0) * Hkv * D;
             pgqa::TileArgs a{q, k_slots[s] + off, v_slots[s] + off, n_span - p0 < tile_len ? n_span - p0 : tile_len,
@@ -591,10 +599,42 @@ int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_
             if ((err = pgqa::launch_tile_update(a, compute_stream)) != cudaSuccess)
                 return cuda_fail(err, "attn_host_tiled_run: tile update");
         }
+        if (traced && (err = cudaEventRecord(trace[4 * g + 3], compute_stream)) != cudaSuccess)
+            return cuda_fail(err, "attn_host_tiled_run: trace event (update end)");
         if ((err = cudaEventRecord(compute_done[s], compute_stream)) != cudaSuccess)
             return cuda_fail(err, "attn_host_tiled_run: cudaEventRecord(compute)");
     }
     return attn_tile_finalize(m, l, acc, B, Hq, D, out_f32, out_bf16, compute_stream);
+}
+
+int attn_host_tiled_run(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v,
+                        int T, int B, int Hq, int Hkv, int D, float scale, int tile_len,
+                        int tiles_per_copy, int n_slots, pgqa_bf16 *const *k_slots,
+                        pgqa_bf16 *const *v_slots, cudaEvent_t const *events, float *m, float *l,
+                        float *acc, float *out_f32, pgqa_bf16 *out_bf16, cudaStream_t compute_stream,
+                        cudaStream_t copy_stream)
+{
+    return host_tiled_impl("attn_host_tiled_run", q, host_k, host_v, T, B, Hq, Hkv, D, scale, tile_len,
+                           tiles_per_copy, n_slots, k_slots, v_slots, events, m, l, acc, out_f32, out_bf16,
+                           compute_stream, copy_stream, nullptr, 0);
+}
+
+int attn_host_tiled_run_traced(const pgqa_bf16 *q, const pgqa_bf16 *host_k, const pgqa_bf16 *host_v, int T,
+                               int B, int Hq, int Hkv, int D, float scale, int tile_len, int tiles_per_copy,
+                               int n_slots, pgqa_bf16 *const *k_slots, pgqa_bf16 *const *v_slots,
+                               cudaEvent_t const *events, float *m, float *l, float *acc, float *out_f32,
+                               pgqa_bf16 *out_bf16, cudaStream_t compute_stream, cudaStream_t copy_stream,
+                               cudaEvent_t const *trace_events, int n_trace_groups)
+{
+    const char *fn = "attn_host_tiled_run_traced";
+    if (n_trace_groups < 0 || (n_trace_groups > 0 && !trace_events))
+        return fail(PGQA_ERR_INVALID_ARG, "%s: trace_events must hold 4 * n_trace_groups events", fn);
+    for (int i = 0; i < 4 * n_trace_groups; ++i)
+        if (!trace_events[i])
+            return fail(PGQA_ERR_INVALID_ARG, "%s: trace event %d is NULL", fn, i);
+    return host_tiled_impl(fn, q, host_k, host_v, T, B, Hq, Hkv, D, scale, tile_len, tiles_per_copy, n_slots,
+                           k_slots, v_slots, events, m, l, acc, out_f32, out_bf16, compute_stream, copy_stream,
+                           trace_events, n_trace_groups);
 }
 
 int attn_host_direct_partition_count(int B, int Hkv, int T, int num_partitions)

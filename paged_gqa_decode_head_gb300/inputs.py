@@ -246,14 +246,18 @@ def qwen3_layers_multi(layers: int | None = None):
     return out
 
 
-def ragged_b64():
-    """Batched ragged decode: B=64, T_b ~ U[1, 32768], one shared page pool."""
+def ragged_b64(batch: int | None = None):
+    """Batched ragged decode: B=64, T_b ~ U[1, 32768], one shared page pool.
+    `batch` keeps only the first sequences of the same draw (a smaller case
+    of the same workload, for profiling captures)."""
     w = WORKLOADS["ragged_b64"]
     ctx = ragged_lengths(w["seed"], w["B"], w["T_lo"], w["T_hi"])
+    q = query(w["seed"], w["B"], w["Hq"], w["D"])
+    if batch is not None:
+        ctx, q = ctx[:batch], q[:batch]
     max_pages = (w["T_hi"] + w["page_size"] - 1) // w["page_size"]
     kv = paged_kv(w["seed"], ctx, Hkv=w["Hkv"], D=w["D"], page_size=w["page_size"], max_pages=max_pages,
                   fill_unused="normal")
-    q = query(w["seed"], w["B"], w["Hq"], w["D"])
     return kv, q
 
 

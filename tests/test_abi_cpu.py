@@ -110,6 +110,10 @@ def test_prologue_and_tile_validation(lib):
                                    *([None] * 10)) == -1  # tiles_per_copy < 1
     assert lib.attn_host_tiled_run(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 65, 2,
                                    *([None] * 10)) == -1  # tiles_per_copy > 64
+    assert lib.attn_host_tiled_run_traced(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 1, 2,
+                                          *([None] * 10), None, -1) == -1  # negative trace count
+    assert lib.attn_host_tiled_run_traced(*([None] * 3), 100, 1, 16, 8, 128, ctypes.c_float(0.1), 512, 1, 2,
+                                          *([None] * 10), None, 2) == -1  # events missing
     del P
 
 

@@ -414,7 +414,7 @@ def test_tile_state_resumes_like_a_checkpoint():
         assert np.abs(out.cpu().numpy() - ref).max() <= ATOL_F32
 
 
-def host_tiled(q, k, v, tile=512, n_slots=2, tiles_per_copy=1):
+def host_tiled(q, k, v, tile=512, n_slots=2, tiles_per_copy=1, trace_events=None):
     dev = "cuda"
     B, Hq, D = q.shape
     _, T, Hkv, _ = k.shape
@@ -432,9 +432,28 @@ def host_tiled(q, k, v, tile=512, n_slots=2, tiles_per_copy=1):
     copy_stream = torch.cuda.Stream()
     pg.attn_host_tiled_run(to_device_bf16(q, dev), hk, hv, SCALE, slots_k, slots_v, events, m, l, acc,
                            out_f32=out, out_bf16=outb, tile_len=tile, tiles_per_copy=tiles_per_copy,
-                           copy_stream=copy_stream)
+                           copy_stream=copy_stream, trace_events=trace_events)
     torch.cuda.synchronize()
     return out.cpu().numpy(), bf16_bits(outb)
+
+
+@pytest.mark.parametrize("per_copy", [1, 4])
+def test_host_tiled_run_traced_gives_the_same_bits_and_ordered_events(per_copy):
+    """The traced pipeline computes exactly what the plain one does; its
+    events, per copy group, come in the order copy start <= copy end <=
+    update start <= update end, and a group's update starts after its copy."""
+    T, tile = 3000, 512
+    k, v = inputs.contiguous_kv(97, 1, T, 8)
+    q = inputs.query(97, 1, 16)
+    plain = host_tiled(q, k, v, tile, 2, per_copy)
+    groups = -(-T // (tile * per_copy))
+    trace = [torch.cuda.Event(enable_timing=True) for _ in range(4 * groups)]
+    traced = host_tiled(q, k, v, tile, 2, per_copy, trace_events=trace)
+    assert np.array_equal(plain[0], traced[0]) and np.array_equal(plain[1], traced[1])
+    t = [trace[0].elapsed_time(ev) for ev in trace]
+    for g in range(groups):
+        c0, c1, u0, u1 = t[4 * g:4 * g + 4]
+        assert 0.0 <= c0 <= c1 <= u0 <= u1
 
 
 @pytest.mark.parametrize("B,T,tile,n_slots,per_copy", [

@@ -323,6 +323,15 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *addr, unsig
     return old;
 }
 
+// 32-bit global load kept where it is written, so that several independent
+// loads issued one after another are in flight together.
+__device__ __forceinline__ int ldg_i32_now(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Block until the grids this one depends on have completed and their memory
 // is visible (no-op when launched without a programmatic dependency).
@@ -336,5 +345,42 @@ __device__ __forceinline__ void allow_dependent_launch()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+
+// Timeline builds (-DPGQA_TIMELINE, a separate library made by the package's
+// timeline module) stamp %globaltimer at each phase of the split kernels
+// (bf16 and INT8; their parameter structs carry `tl` and `tl_launch`) into a
+// caller buffer [launch][CTA][kTimelineSlots]; other builds compile the
+// stamps out. Slots: 0 CTA start, 1 block-table entries in hand, 2 first
+// requests issued, 3 grid dependency released, 4 query rotated (fused step),
+// 5 a warp's second chunk landed, 6 last chunk landed (latest warp), 7 warp
+// records merged, 8 partition state written, 9 ticket back, 10 merge done.
+constexpr int kTimelineSlots = 12;
+#ifdef PGQA_TIMELINE
+// host side (decode.cu): the attached buffer and the next launch's slot
+unsigned long long *timeline_buffer();
+int timeline_next_launch();
+#define TL_INDEX(slot)                                                                                       \
+    ((static_cast<size_t>(p.tl_launch) * gridDim.x * gridDim.y * gridDim.z + blockIdx.x +                     \
+      gridDim.x * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z)) *                                \
+         kTimelineSlots +                                                                                     \
+     (slot))
+#define TL_STAMP(slot)                                                                                       \
+    do {                                                                                                     \
+        if (p.tl && threadIdx.x == 0)                                                                        \
+            p.tl[TL_INDEX(slot)] = globaltimer_ns();                                                         \
+    } while (0)
+#define TL_STAMP_LATEST(slot)                                                                                \
+    do {                                                                                                     \
+        if (p.tl && (threadIdx.x & 31) == 0)                                                                 \
+            atomicMax(&p.tl[TL_INDEX(slot)], globaltimer_ns());                                              \
+    } while (0)
+#else
+#define TL_STAMP(slot) \
+    do {               \
+    } while (0)
+#define TL_STAMP_LATEST(slot) \
+    do {                      \
+    } while (0)
+#endif
 
 } // namespace pgqa

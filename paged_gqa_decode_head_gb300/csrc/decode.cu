@@ -59,41 +59,6 @@ __device__ unsigned g_flags_decode;
 
 __device__ __forceinline__ void raise_flag(unsigned f) { atomicOr(&g_flags_decode, f); }
 
-// Timeline builds (-DPGQA_TIMELINE, a separate library made by the package's
-// timeline module) stamp %globaltimer at each phase of the split kernel into
-// a caller buffer [launch][CTA][kTimelineSlots]; other builds compile the
-// stamps out. Slots: 0 CTA start, 1 block-table entries in hand, 2 first
-// requests issued, 3 grid dependency released, 4 query rotated (fused step),
-// 5 a warp's second chunk landed, 6 last chunk landed (latest warp), 7 warp
-// records merged, 8 partition state written, 9 ticket back, 10 merge done.
-constexpr int kTimelineSlots = 12;
-#ifdef PGQA_TIMELINE
-unsigned long long *g_timeline_buf = nullptr; // host copy of the attached buffer
-int g_timeline_launches = 1, g_timeline_next = 0;
-#define TL_INDEX(slot)                                                                                       \
-    ((static_cast<size_t>(p.tl_launch) * gridDim.x * gridDim.y * gridDim.z + blockIdx.x +                     \
-      gridDim.x * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z)) *                                \
-         kTimelineSlots +                                                                                     \
-     (slot))
-#define TL_STAMP(slot)                                                                                       \
-    do {                                                                                                     \
-        if (p.tl && threadIdx.x == 0)                                                                        \
-            p.tl[TL_INDEX(slot)] = globaltimer_ns();                                                         \
-    } while (0)
-#define TL_STAMP_LATEST(slot)                                                                                \
-    do {                                                                                                     \
-        if (p.tl && (threadIdx.x & 31) == 0)                                                                 \
-            atomicMax(&p.tl[TL_INDEX(slot)], globaltimer_ns());                                              \
-    } while (0)
-#else
-#define TL_STAMP(slot) \
-    do {               \
-    } while (0)
-#define TL_STAMP_LATEST(slot) \
-    do {                      \
-    } while (0)
-#endif
-
 constexpr int kBoxBytes = kChunkTokens * 128;   // 16 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kBoxBytes;      // K lo, K hi, V lo, V hi
 constexpr int kFusedMergeMax = 64;              // partitions the last CTA merges itself
@@ -1140,9 +1105,8 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
 #ifdef PGQA_TIMELINE
-    kp.tl = g_timeline_buf;
-    kp.tl_launch = g_timeline_next;
-    g_timeline_next = (g_timeline_next + 1) % g_timeline_launches;
+    kp.tl = timeline_buffer();
+    kp.tl_launch = timeline_next_launch();
 #endif
     const bool pair = use_pair_shape(NCOL, M, a.B, a.Hkv, a.num_partitions, a.pages_per_part * a.page_size,
                                      a.sm_count);
@@ -1255,9 +1219,22 @@ cudaError_t launch_wait_selftest(cudaStream_t stream)
 }
 
 #ifdef PGQA_TIMELINE
+unsigned long long *g_timeline_buf = nullptr; // the attached buffer
+int g_timeline_launches = 1, g_timeline_next = 0;
+
+unsigned long long *timeline_buffer() { return g_timeline_buf; }
+
+int timeline_next_launch()
+{
+    const int i = g_timeline_next;
+    g_timeline_next = (g_timeline_next + 1) % g_timeline_launches;
+    return i;
+}
+
 // Attach (or, with NULL, detach) the timeline buffer: `launches` slots of
 // [CTAs][kTimelineSlots] u64, filled in turn by the following split-kernel
-// launches (captured graphs keep the slot they were captured with).
+// launches of either kernel (captured graphs keep the slot they were
+// captured with).
 extern "C" int pgqa_timeline_attach(unsigned long long *buf, int launches)
 {
     g_timeline_buf = buf;

@@ -116,6 +116,9 @@ struct Int8Params {
     unsigned *tickets; // [B*Hkv] partition tickets (in-kernel merge)
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
     int fused_merge;
+    // 1: tmap_k spans both code caches (one TMA load per chunk's K and V
+    // tiles); 1: tmap_s spans both scale arrays (one load per chunk's scales)
+    int kv_map, scale_map;
     float scale_log2;
     // fused decode step only: the new token's raw heads, the prologue's
     // parameters and the cache to append to
@@ -125,6 +128,10 @@ struct Int8Params {
     uint16_t *q_out;
     float eps;
     RopeFreqs freqs;
+#ifdef PGQA_TIMELINE
+    unsigned long long *tl; // timeline buffer, or NULL
+    int tl_launch;          // this launch's index in it
+#endif
 };
 
 // Per-warp online-softmax state on fp16 MMA fragments (transposed as in the
@@ -353,7 +360,7 @@ template <int G> struct Int8Warp {
 template <int G, bool kFused, typename S>
 __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     decode_int8_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                       const Int8Params p)
+                       const __grid_constant__ CUtensorMap tmap_s, const Int8Params p)
 {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -363,6 +370,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     const int part = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
 
     allow_dependent_launch();
+    TL_STAMP(0);
     unsigned char *stages = smem + warp * S::kStages * kStage8;
     float *scales = reinterpret_cast<float *>(smem + S::kScaleOffset) + warp * S::kStages * 2 * kChunkTokens;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset) + warp * S::kStages;
@@ -371,6 +379,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
         if (warp == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
+            prefetch_tensormap(&tmap_s);
         }
 #pragma unroll
         for (int s = 0; s < S::kStages; ++s)
@@ -382,7 +391,17 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     const int tok0 = part * part_tokens;
     const int32_t *table = p.block_table + static_cast<size_t>(b) * p.max_pages;
     auto chunk_token = [&](int k) { return tok0 + (warp + k * S::kWarps) * kChunkTokens; };
-    int T = p.context_lens[b];
+    // The first 32 table entries of this warp's chunks are loaded before the
+    // context length is known (any entry below max_pages may be read), both
+    // loads issued where they stand, so the first requests wait for one
+    // memory round trip, not two.
+    int tbl_blk = 0, tbl_val = -1;
+    {
+        const int page = chunk_token(lane) / p.P;
+        if (chunk_token(lane) < tok0 + part_tokens && page < p.max_pages)
+            tbl_val = ldg_i32_now(table + page);
+    }
+    int T = ldg_i32_now(p.context_lens + b);
     if (T < (kFused ? 1 : 0) || T > p.max_pages * p.P) {
         if (part == 0 && threadIdx.x == 0)
             raise_flag8(PGQA_DEVERR_BAD_CONTEXT);
@@ -404,7 +423,6 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     auto holds_new_token = [&](int k) { return !kFused && chunk_token(k) + kChunkTokens > T - 1; };
     // Physical pages of this warp's chunks, 32 at a time: lane L caches the
     // entry of chunk 32*blk + L. Called by the whole (converged) warp.
-    int tbl_blk = -1, tbl_val = -1;
     auto phys_of = [&](int k) {
         if ((k >> 5) != tbl_blk) {
             tbl_blk = k >> 5;
@@ -427,10 +445,18 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
         unsigned char *dst = stages + (k % S::kStages) * kStage8;
         float *sdst = scales + (k % S::kStages) * 2 * kChunkTokens;
         mbar_arrive_expect_tx(bar, kStage8 + kScaleBytes8);
-        tma_load_2d(dst, &tmap_k, 0, row, bar, policy);
-        tma_load_2d(dst + kTile8, &tmap_v, 0, row, bar, policy);
-        bulk_copy_g2s(sdst, p.k_scale + row, kChunkTokens * 4, bar, policy);
-        bulk_copy_g2s(sdst + kChunkTokens, p.v_scale + row, kChunkTokens * 4, bar, policy);
+        if (p.kv_map) {
+            tma_load_3d(dst, &tmap_k, 0, row, 0, bar, policy);
+        } else {
+            tma_load_2d(dst, &tmap_k, 0, row, bar, policy);
+            tma_load_2d(dst + kTile8, &tmap_v, 0, row, bar, policy);
+        }
+        if (p.scale_map) {
+            tma_load_2d(sdst, &tmap_s, row, 0, bar, policy);
+        } else {
+            bulk_copy_g2s(sdst, p.k_scale + row, kChunkTokens * 4, bar, policy);
+            bulk_copy_g2s(sdst + kChunkTokens, p.v_scale + row, kChunkTokens * 4, bar, policy);
+        }
     };
 
     const uint64_t policy = l2_evict_first_policy();
@@ -439,12 +465,14 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
 #pragma unroll
     for (int k = 0; k < S::kStages; ++k)
         first_phys[k] = k < first ? phys_of(k) : -1;
+    TL_STAMP(1);
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < S::kStages; ++k)
             if (k < first && k < S::template kPrewait<kFused> && !holds_new_token(k))
                 issue(k, first_phys[k], policy);
     }
+    TL_STAMP(2);
 
     // fused step: warps < G rotate the query heads; the warp owning the chunk
     // of position T-1 quantizes and appends the new K and V rows. What no
@@ -470,6 +498,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
         load_head(p.gamma_k, gain_k);
 
     grid_dependency_wait();
+    TL_STAMP(3);
 
     const size_t row0 = static_cast<size_t>(b) * p.Hq + kvh * G;
     const size_t krow = (static_cast<size_t>(b) * p.Hkv + kvh) * kHeadDim;
@@ -510,6 +539,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
         }
         __syncthreads();
         st.init(q_buf);
+        TL_STAMP(4);
         if (new_chunk >= 0) {
             int kc[4], vc[4];
             norm_rope_apply(xk, gain_k, p.eps, rope);
@@ -563,6 +593,10 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
                 const bool landed = mbar_wait_bounded(&bars[k % S::kStages], (k / S::kStages) & 1);
                 if (!__all_sync(0xFFFFFFFFu, landed))
                     ok = false;
+                if (k == 1)
+                    TL_STAMP(5);
+                if (k == my_chunks - 1)
+                    TL_STAMP_LATEST(6);
                 rows[c] = stage_rows[k % S::kStages];
                 if (kFused && k == new_chunk && rows[c] > 0) {
                     // the staged copy predates the append: put the new row in
@@ -617,6 +651,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     // every copy into this warp's stages has landed: they can hold its record
     st.store_record(reinterpret_cast<float *>(stages));
     __syncthreads();
+    TL_STAMP(7);
 
     for (int e = threadIdx.x; e < G * kHeadDim; e += S::kWarps * 32) {
         const int h = e / kHeadDim, d = e % kHeadDim;
@@ -659,11 +694,13 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     // before the merge's loads, which the second barrier extends to all
     // threads.
     unsigned *ticket_slot = reinterpret_cast<unsigned *>(smem + S::kTicketOffset);
+    TL_STAMP(8);
     __syncthreads();
     unsigned *ticket = p.tickets + static_cast<size_t>(b) * p.Hkv + kvh;
     if (threadIdx.x == 0)
         *ticket_slot = atomic_add_acq_rel_gpu(ticket, 1u);
     __syncthreads();
+    TL_STAMP(9);
     if (*ticket_slot != static_cast<unsigned>(n_parts - 1))
         return;
     const auto row_of = [&](int c) { return row0 + c; };
@@ -672,6 +709,10 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
             reinterpret_cast<uint64_t *>(smem + S::kMergeBarOffset)) &&
         threadIdx.x == 0)
         raise_flag8(PGQA_DEVERR_WAIT_TIMEOUT); // the merge's copy never landed: outputs left alone
+#ifdef PGQA_TIMELINE
+    __syncthreads();
+    TL_STAMP(10);
+#endif
     if (threadIdx.x == 0)
         *ticket = 0u; // ready for the next call
 }
@@ -693,9 +734,52 @@ cudaError_t encode_int8_map(CUtensorMap *map, const void *base, long long rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Both code caches as one 3-D tensor [2 caches][rows][128 bytes] (the
+// outer dimension steps from k_cache8 to v_cache8): one box {128, 16, 2}
+// lands a chunk's K tile and V tile (128-byte swizzle) with one TMA
+// instruction. Needs v_cache8 above k_cache8 by a multiple of 16 bytes.
+cudaError_t encode_int8_kv_map(CUtensorMap *map, const void *k_base, const void *v_base, long long rows)
+{
+    const uintptr_t k = reinterpret_cast<uintptr_t>(k_base), v = reinterpret_cast<uintptr_t>(v_base);
+    if (v <= k || (v - k) % 16 != 0 || v - k >= (1ull << 40))
+        return cudaErrorInvalidValue;
+    EncodeTiledFn fn = tensor_map_encoder();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {128u, static_cast<cuuint64_t>(rows), 2u};
+    const cuuint64_t strides[2] = {128u, static_cast<cuuint64_t>(v - k)};
+    const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(kChunkTokens), 2u};
+    const cuuint32_t elem[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(k_base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Both scale arrays as one 2-D tensor [2 arrays][rows] fp32: one box
+// {16, 2} lands a chunk's 16 K scales and 16 V scales. Needs v_scale above
+// k_scale by a multiple of 16 bytes.
+cudaError_t encode_scale_map(CUtensorMap *map, const float *k_scale, const float *v_scale, long long rows)
+{
+    const uintptr_t k = reinterpret_cast<uintptr_t>(k_scale), v = reinterpret_cast<uintptr_t>(v_scale);
+    if (v <= k || (v - k) % 16 != 0 || v - k >= (1ull << 40))
+        return cudaErrorInvalidValue;
+    EncodeTiledFn fn = tensor_map_encoder();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rows), 2u};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(v - k)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunkTokens), 2u};
+    const cuuint32_t elem[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(k_scale), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int G, bool kFused, typename S>
-cudaError_t launch_int8_t(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
-                          cudaStream_t stream)
+cudaError_t launch_int8_t(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &ms,
+                          const Int8Params &kp, dim3 grid, cudaStream_t stream)
 {
     static bool configured[64] = {};
     int dev = 0;
@@ -710,7 +794,7 @@ cudaError_t launch_int8_t(const CUtensorMap &mk, const CUtensorMap &mv, const In
         if (dev < 64)
             configured[dev] = true;
     }
-    return launch_pdl(decode_int8_kernel<G, kFused, S>, grid, dim3(S::kWarps * 32), S::kSmem, stream, mk, mv,
+    return launch_pdl(decode_int8_kernel<G, kFused, S>, grid, dim3(S::kWarps * 32), S::kSmem, stream, mk, mv, ms,
                       kp);
 }
 
@@ -723,24 +807,24 @@ template <typename S> bool merges_in_kernel(int G, int num_partitions)
 enum class Shape8Kind { kShort, kDeep, kPair, kTrio };
 
 template <int G>
-cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const Int8Params &kp, dim3 grid,
-                          bool fused, Shape8Kind shape, cudaStream_t stream)
+cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &ms,
+                          const Int8Params &kp, dim3 grid, bool fused, Shape8Kind shape, cudaStream_t stream)
 {
     if constexpr (G <= Shape8Trio::kWarps) {
         if (shape == Shape8Kind::kTrio)
-            return fused ? launch_int8_t<G, true, Shape8Trio>(mk, mv, kp, grid, stream)
-                         : launch_int8_t<G, false, Shape8Trio>(mk, mv, kp, grid, stream);
+            return fused ? launch_int8_t<G, true, Shape8Trio>(mk, mv, ms, kp, grid, stream)
+                         : launch_int8_t<G, false, Shape8Trio>(mk, mv, ms, kp, grid, stream);
     }
     if constexpr (G <= Shape8Pair::kWarps) {
         if (shape == Shape8Kind::kPair)
-            return fused ? launch_int8_t<G, true, Shape8Pair>(mk, mv, kp, grid, stream)
-                         : launch_int8_t<G, false, Shape8Pair>(mk, mv, kp, grid, stream);
+            return fused ? launch_int8_t<G, true, Shape8Pair>(mk, mv, ms, kp, grid, stream)
+                         : launch_int8_t<G, false, Shape8Pair>(mk, mv, ms, kp, grid, stream);
     }
     if (shape == Shape8Kind::kDeep)
-        return fused ? launch_int8_t<G, true, Shape8Deep>(mk, mv, kp, grid, stream)
-                     : launch_int8_t<G, false, Shape8Deep>(mk, mv, kp, grid, stream);
-    return fused ? launch_int8_t<G, true, Shape8Short>(mk, mv, kp, grid, stream)
-                 : launch_int8_t<G, false, Shape8Short>(mk, mv, kp, grid, stream);
+        return fused ? launch_int8_t<G, true, Shape8Deep>(mk, mv, ms, kp, grid, stream)
+                     : launch_int8_t<G, false, Shape8Deep>(mk, mv, ms, kp, grid, stream);
+    return fused ? launch_int8_t<G, true, Shape8Short>(mk, mv, ms, kp, grid, stream)
+                 : launch_int8_t<G, false, Shape8Short>(mk, mv, ms, kp, grid, stream);
 }
 
 } // namespace
@@ -750,16 +834,27 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     if (a.B == 0)
         return cudaSuccess;
     const int G = a.Hq / a.Hkv;
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, ms;
     const long long rows = static_cast<long long>(a.num_pages) * a.Hkv * a.page_size;
     if (rows == 0)
         return cudaErrorInvalidValue;
-    cudaError_t err = encode_int8_map(&mk, a.k_cache8, rows);
-    if (err == cudaSuccess)
-        err = encode_int8_map(&mv, a.v_cache8, rows);
-    if (err != cudaSuccess)
-        return err;
     Int8Params kp{};
+    cudaError_t err = encode_int8_kv_map(&mk, a.k_cache8, a.v_cache8, rows);
+    if (err == cudaSuccess) {
+        kp.kv_map = 1;
+        mv = mk;
+    } else {
+        err = encode_int8_map(&mk, a.k_cache8, rows);
+        if (err == cudaSuccess)
+            err = encode_int8_map(&mv, a.v_cache8, rows);
+        if (err != cudaSuccess)
+            return err;
+    }
+    if (encode_scale_map(&ms, a.k_scale, a.v_scale, rows) == cudaSuccess)
+        kp.scale_map = 1;
+    else
+        ms = mk; // unused
+
     kp.q = a.q;
     kp.block_table = a.block_table;
     kp.context_lens = a.context_lens;
@@ -775,6 +870,10 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     kp.NP = a.num_partitions;
     kp.ppp = a.pages_per_part;
     kp.scale_log2 = a.scale * kLog2e;
+#ifdef PGQA_TIMELINE
+    kp.tl = timeline_buffer();
+    kp.tl_launch = timeline_next_launch();
+#endif
     if (a.fused) {
         kp.q_raw = a.q_raw;
         kp.k_new = a.k_new;
@@ -818,14 +917,14 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     }
     const dim3 grid(a.num_partitions, a.Hkv, a.B);
     switch (G) {
-    case 1: err = launch_int8_g<1>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 2: err = launch_int8_g<2>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 3: err = launch_int8_g<3>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 4: err = launch_int8_g<4>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 5: err = launch_int8_g<5>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 6: err = launch_int8_g<6>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 7: err = launch_int8_g<7>(mk, mv, kp, grid, a.fused, shape, stream); break;
-    case 8: err = launch_int8_g<8>(mk, mv, kp, grid, a.fused, shape, stream); break;
+    case 1: err = launch_int8_g<1>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 2: err = launch_int8_g<2>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 3: err = launch_int8_g<3>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 4: err = launch_int8_g<4>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 5: err = launch_int8_g<5>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 6: err = launch_int8_g<6>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 7: err = launch_int8_g<7>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
+    case 8: err = launch_int8_g<8>(mk, mv, ms, kp, grid, a.fused, shape, stream); break;
     default: return cudaErrorInvalidValue;
     }
     if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)

@@ -9,7 +9,11 @@ CTAs, averaged over layers 4..27 and several replays. The stamps themselves
 cost a little: the instrumented step runs a few tenths of a microsecond
 slower per layer than the plain library, which the tool reports beside it.
 
-    python -m paged_gqa_decode_head_gb300.timeline [--replays 10] [--partitions 0]
+    python -m paged_gqa_decode_head_gb300.timeline [--replays 10] [--partitions 0] [--int8]
+
+--int8 runs the same chain over an INT8 cache (decode_step_paged_int8 and
+decode_attn_paged_int8; codes uniform in [-127, 127], scales 1/127, as the
+benchmark's INT8 chain).
 """
 from __future__ import annotations
 
@@ -62,10 +66,85 @@ def summarise(d, first_layer: int = 4):
     return out, float(np.mean(lens))
 
 
+class Int8Chain:
+    """The 28-layer T = 8192 chain over INT8 caches, with DecodeStep's
+    partitions and capture() interface (the benchmark's INT8 leg)."""
+
+    def __init__(self, layers: int, num_partitions: int):
+        import torch
+
+        from . import binding, inputs
+        from .runner import to_device_bf16, to_device_i32
+
+        w = inputs.WORKLOADS["qwen3_0p6b_t8k_int8"]
+        self.w = w
+        self.num_partitions = num_partitions
+        self.bufs = []
+        for i in range(layers):
+            seed = w["seed"] * 1000 + i
+            kv = inputs.paged_kv(seed, [w["T"]] * w["B"], Hkv=w["Hkv"], page_size=w["page_size"], spare_pages=0,
+                                 fill_unused="normal")
+            tok = inputs.new_token(seed, w["B"], w["Hq"], w["Hkv"])
+            self.bufs.append(dict(
+                k8=torch.from_numpy(inputs.int8_rows(seed, kv.k_cache.shape, 70)).cuda(),
+                v8=torch.from_numpy(inputs.int8_rows(seed, kv.v_cache.shape, 71)).cuda(),
+                ks=torch.full(kv.k_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device="cuda"),
+                vs=torch.full(kv.v_cache.shape[:-1], 1.0 / 127, dtype=torch.float32, device="cuda"),
+                bt=to_device_i32(kv.block_table, "cuda"), ctx=to_device_i32(kv.context_lens, "cuda"),
+                q=to_device_bf16(tok.q, "cuda"), k=to_device_bf16(tok.k, "cuda"), v=to_device_bf16(tok.v, "cuda"),
+                gq=to_device_bf16(tok.gamma_q, "cuda"), gk=to_device_bf16(tok.gamma_k, "cuda"),
+                q_out=torch.empty((w["B"], w["Hq"], 128), dtype=torch.bfloat16, device="cuda"),
+                out=torch.empty((w["B"], w["Hq"], 128), dtype=torch.float32, device="cuda"),
+                P=kv.page_size, mp=kv.max_pages))
+        b0 = self.bufs[0]
+        n = binding.decode_attn_int8_workspace_size(w["B"], w["Hq"], w["Hkv"], 128, b0["P"], b0["mp"],
+                                                     num_partitions)
+        self.ws = torch.zeros(max(16, n), dtype=torch.uint8, device="cuda")
+
+    @property
+    def partitions(self) -> int:
+        from . import binding
+
+        b0 = self.bufs[0]
+        return binding.decode_attn_partition_count(self.w["B"], self.w["Hkv"], b0["P"], b0["mp"],
+                                                   self.num_partitions)
+
+    def run(self, fused: bool):
+        import math
+
+        from . import binding
+
+        scale = 1.0 / math.sqrt(128)
+        for b_ in self.bufs:
+            if fused:
+                binding.decode_step_paged_int8(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                               b_["k8"], b_["v8"], b_["ks"], b_["vs"], scale, self.w["theta"],
+                                               q_out=b_["q_out"], out_f32=b_["out"], workspace=self.ws,
+                                               num_partitions=self.num_partitions)
+            else:
+                binding.decode_attn_paged_int8(b_["q"], b_["k8"], b_["v8"], b_["ks"], b_["vs"], b_["bt"], b_["ctx"],
+                                               scale, out_f32=b_["out"], workspace=self.ws,
+                                               num_partitions=self.num_partitions)
+
+    def capture(self, prologue: bool = True, fused: bool = False):
+        import torch
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run(fused)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(fused)
+        return g
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--replays", type=int, default=10)
     ap.add_argument("--partitions", type=int, default=0, help="0: the library's automatic count")
+    ap.add_argument("--int8", action="store_true", help="the INT8 cache's step and attention instead of bf16")
     ap.add_argument("--library", default=None,
                     help="an already built timeline library (default: build libpgqa_timeline.so here)")
     args = ap.parse_args(argv)
@@ -82,8 +161,9 @@ def main(argv=None):
     slots = lib.pgqa_timeline_attach(None, 1)
     L = 28
     w = inputs.WORKLOADS["qwen3_0p6b_t8k"]
-    step = DecodeStep(inputs.qwen3_layers(layers=L), Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"],
-                      num_partitions=args.partitions)
+    step = Int8Chain(L, args.partitions) if args.int8 else DecodeStep(
+        inputs.qwen3_layers(layers=L), Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"],
+        num_partitions=args.partitions)
     np_used = step.partitions
     grid = np_used * w["Hkv"]
     buf = torch.zeros(L * grid * slots, dtype=torch.int64, device="cuda")
@@ -91,6 +171,8 @@ def main(argv=None):
     keep = []
     for fused in (True, False):
         name = "fused step (decode_step_paged)" if fused else "attention alone (decode_attn_paged)"
+        if args.int8:
+            name = name.replace("paged)", "paged_int8)")
         lib.pgqa_timeline_attach(None, 1)
         plain = step.capture(prologue=fused, fused=fused)
         # the capture's warm-up run takes the first L launch slots, the

@@ -12,12 +12,13 @@
 // float [num_pages][Hkv][P] for K and for V.
 //
 // GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
-// kW-th 16-position chunk of the partition and a private ring of stages (9
-// warps x 6 stages for short partitions, 12 warps x 4 for long ones, and
+// kW-th 16-position chunk of the partition and a private ring of stages (12
+// warps x 3 stages for short partitions, 12 warps x 4 for long ones, and
 // three or two CTAs per SM of 4 or 6 warps x 4 for grids of several waves
-// with short partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V: 16 rows x 128 bytes,
-// 128-byte swizzle) plus the chunk's 2 x 64 bytes of scales by bulk copy, all
-// completing on one mbarrier. The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
+// with short partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V:
+// 16 rows x 128 bytes, 128-byte swizzle) plus the chunk's 2 x 64 bytes of
+// scales, all completing on one mbarrier (one TMA load for both tiles and
+// one for both scale rows when the caller's buffers allow it). The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
 // converted in registers: ldmatrix hands a lane four consecutive bytes of a
 // row, so the MMA's k index (S^T = K Q^T) and M index (O^T = V^T P^T) are
 // taken in a fixed permutation of the 16 dims of a step -- the query is loaded
@@ -65,7 +66,9 @@ template <int kW, int kS, int kCtas> struct Shape8 {
     static constexpr int kWarps = kW;
     static constexpr int kStages = kS;
     static constexpr int kCtasPerSm = kCtas;
-    static constexpr int kGroup = kStages / 2; // chunks folded together
+    // chunks folded together: half the ring (one half loads while the other
+    // folds), and at least a pair when the ring has room for one
+    static constexpr int kGroup = kStages >= 4 ? kStages / 2 : (kStages >= 2 ? 2 : 1);
     static constexpr int kStageArea = kWarps * kStages * kStage8;
     static constexpr int kScaleOffset = kStageArea;
     static constexpr int kBarOffset = kScaleOffset + kWarps * kStages * kScaleBytes8;
@@ -80,16 +83,22 @@ template <int kW, int kS, int kCtas> struct Shape8 {
     static constexpr int kSmem = 1024 /* alignment slack */ + kPatchOffset + 2 * kHeadDim + 16;
     static constexpr int kMergeScratch = merge_scratch_bytes<kWarps * 32, kFusedMergeMax8>(kMaxGroup);
     // chunks per warp requested before griddepcontrol.wait: all of the ring
-    // (the fused step on the T = 8192 chain: 9.11 us per layer with all
-    // stages, 9.20 with 4, 9.32 with 3, 9.59 with 2)
+    // (the fused step on the T = 8192 chain with 9 warps x 6 stages: 9.11 us
+    // per layer with all stages, 9.20 with 4, 9.32 with 3, 9.59 with 2)
     template <bool kFused> static constexpr int kPrewait = kStages;
     static_assert(kSmem <= 232448, "exceeds the 227 KiB of shared memory a CTA may hold");
     static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
     static_assert(kGroup >= 1 && kGroup <= 3, "fold groups of 1 to 3 chunks");
 };
-// 9 warps x 6 stages suit short partitions in one wave (the T = 8192 layer
-// chain: 3 chunks per warp, all in flight at once).
-using Shape8Short = Shape8<9, 6, 1>;
+// 12 warps x 3 stages for short partitions in one wave (the T = 8192 layer
+// chain: up to 3 chunks per warp, all in flight at once). The chain's time
+// after the query arrives is the fold of every chunk of the partition, which
+// is issue-bound: three warps per SM sub-partition instead of 9 warps (one
+// sub-partition with three, the others two) fold it sooner. 28-layer chain,
+// same process: fused step 8.11 us per layer against 8.64 for 9 x 6 and
+// 8.08 for 12 x 4 (attention alone 7.84, 8.34, 7.91); 3 stages take less
+// shared memory than 4 for the same time.
+using Shape8Short = Shape8<12, 3, 1>;
 // 12 warps x 4 stages spread evenly over the SM's four sub-partitions (9
 // warps leave one of them with three), which long partitions, bound by the
 // fold, need.
@@ -577,7 +586,7 @@ __global__ void __launch_bounds__(S::kWarps * 32, S::kCtasPerSm)
     int k0 = 0;
     // As in the bf16 kernel: pairs for warps with few chunks, whole groups
     // otherwise (the grouping depends only on the chunk count).
-    const int group = my_chunks <= 2 * S::kGroup ? 2 : S::kGroup;
+    const int group = min(S::kGroup, my_chunks <= 2 * S::kGroup ? 2 : S::kGroup);
     for (int nc; k0 < my_chunks; k0 += nc) {
         nc = min(group, my_chunks - k0);
         uint32_t stage_addr[S::kGroup];
@@ -890,8 +899,8 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
     }
     // Grids of more than one wave (of one CTA per SM) with short partitions
     // take three or two CTAs per SM (the fused step and attention alone
-    // alike, so they give equal bits); otherwise long partitions take the
-    // 12-warp shape (fold-bound), short ones 9 warps.
+    // alike, so they give equal bits); otherwise long partitions take 12
+    // warps x 4 stages, short ones 12 warps x 3 (both fold-bound).
     const long part_positions = static_cast<long>(a.pages_per_part) * a.page_size;
     const bool waves = a.num_partitions > 1 &&
                        static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);

@@ -356,3 +356,50 @@ def test_int8_fused_step_full_size_t8192():
     for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
         assert np.array_equal(a, b), name
     assert pg.device_error_flags() == 0
+
+
+def _carved(first, second):
+    """Two device tensors carved from one allocation, `first` at the lower
+    address (so the order of the code caches and of the scale arrays in
+    memory is fixed)."""
+    a = np.ascontiguousarray(first)
+    b = np.ascontiguousarray(second)
+    buf = torch.from_numpy(np.concatenate([a.reshape(-1).view(np.uint8), b.reshape(-1).view(np.uint8)])).cuda()
+    n = a.nbytes
+    return (buf[:n].view(torch.int8 if a.dtype == np.int8 else torch.float32).view(a.shape),
+            buf[n:].view(torch.int8 if b.dtype == np.int8 else torch.float32).view(b.shape))
+
+
+@pytest.mark.parametrize("v_first", [False, True])
+def test_int8_attention_with_either_order_of_the_caches_in_memory(v_first):
+    """V above K in memory lets one copy fetch a chunk's K and V codes (and
+    one its scales); V below K takes the separate copies. Both give the
+    same bits, and the oracle's attention."""
+    kv = inputs.paged_kv(1190, [3000, 700], Hkv=8, page_size=16, fill_unused="normal")
+    q = inputs.query(1190, 2, 16)
+    k8, v8, ks, vs = int8_cache(kv)
+    B, Hq = 2, 16
+    if v_first:
+        v8d, k8d = _carved(v8, k8)
+        vsd, ksd = _carved(vs, ks)
+    else:
+        k8d, v8d = _carved(k8, v8)
+        ksd, vsd = _carved(ks, vs)
+    outs = []
+    for npr in (0, 5):
+        n = pg.decode_attn_int8_workspace_size(B, Hq, 8, 128, kv.page_size, kv.max_pages, npr)
+        ws = torch.zeros(max(16, n), dtype=torch.uint8, device="cuda")
+        of = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+        pg.decode_attn_paged_int8(to_device_bf16(q, "cuda"), k8d, v8d, ksd, vsd, to_device_i32(kv.block_table, "cuda"),
+                                  to_device_i32(kv.context_lens, "cuda"), SCALE, out_f32=of, workspace=ws,
+                                  num_partitions=npr)
+        torch.cuda.synchronize()
+        outs.append(of.cpu().numpy())
+    ref = oracle.decode_attention_int8(q, k8, v8, ks, vs, kv.block_table, kv.context_lens, SCALE)
+    for o in outs:
+        assert np.abs(o - ref).max() <= ATOL_F32
+    # the same bits as the default allocation (each cache its own tensor)
+    for o, npr in zip(outs, (0, 5)):
+        of, _ = run_attention(kv, q, k8, v8, ks, vs, npr)
+        assert np.array_equal(o, of)
+    assert pg.device_error_flags() == 0

@@ -13,8 +13,8 @@
 //
 // GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
 // kW-th 16-position chunk of the partition and a private ring of stages (12
-// warps x 3 stages for short partitions, 12 warps x 4 for long ones, and
-// three or two CTAs per SM of 4 or 6 warps x 4 for grids of several waves
+// warps x 3 stages for short partitions, 16 warps x 3 for long ones, and
+// four or two CTAs per SM of 4 or 8 warps x 3 for grids of several waves
 // with short partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V:
 // 16 rows x 128 bytes, 128-byte swizzle) plus the chunk's 2 x 64 bytes of
 // scales, all completing on one mbarrier (one TMA load for both tiles and
@@ -56,19 +56,19 @@ constexpr int kTile8 = kChunkTokens * 128;         // 16 rows x 128 int8 codes
 constexpr int kStage8 = 2 * kTile8;                // K tile, V tile
 constexpr int kScaleBytes8 = 2 * kChunkTokens * 4; // K scales, V scales
 constexpr int kFusedMergeMax8 = 64;                // partitions the last CTA merges itself
-// Partitions of at least this many chunks use the 12-warp shape.
+// Partitions of at least this many chunks use the 16-warp shape.
 constexpr int kDeepChunks8 = 64;
 
 // CTA shapes: kW warps, each owning every kW-th chunk of its partition in a
-// ring of kS stages folded kGroup at a time (two groups: one loads while the
-// other folds), kCtas CTAs per SM.
-template <int kW, int kS, int kCtas> struct Shape8 {
+// ring of kS stages folded kGroup at a time, kCtas CTAs per SM.
+template <int kW, int kS, int kCtas, int kGrp = 0> struct Shape8 {
     static constexpr int kWarps = kW;
     static constexpr int kStages = kS;
     static constexpr int kCtasPerSm = kCtas;
-    // chunks folded together: half the ring (one half loads while the other
-    // folds), and at least a pair when the ring has room for one
-    static constexpr int kGroup = kStages >= 4 ? kStages / 2 : (kStages >= 2 ? 2 : 1);
+    // chunks folded together: kGrp if given, else half the ring (one half
+    // loads while the other folds), and at least a pair when the ring has
+    // room for one
+    static constexpr int kGroup = kGrp ? kGrp : (kStages >= 4 ? kStages / 2 : (kStages >= 2 ? 2 : 1));
     static constexpr int kStageArea = kWarps * kStages * kStage8;
     static constexpr int kScaleOffset = kStageArea;
     static constexpr int kBarOffset = kScaleOffset + kWarps * kStages * kScaleBytes8;
@@ -99,21 +99,29 @@ template <int kW, int kS, int kCtas> struct Shape8 {
 // 8.08 for 12 x 4 (attention alone 7.84, 8.34, 7.91); 3 stages take less
 // shared memory than 4 for the same time.
 using Shape8Short = Shape8<12, 3, 1>;
-// 12 warps x 4 stages spread evenly over the SM's four sub-partitions (9
-// warps leave one of them with three), which long partitions, bound by the
-// fold, need.
-using Shape8Deep = Shape8<12, 4, 1>;
+// Long partitions are bound by the fold's latency: a warp issues about once
+// in 5.4 cycles (MMA and conversion chains), so the SM wants four warps on
+// each of its sub-partitions, i.e. 16 warps (the most that fit 128
+// registers a thread), each folding one chunk at a time while its other two
+// stages load. B = 1, Hq = 32, T = 131072, 19 partitions, same process
+// (us): 16 x 3 one at a time 45.7, 16 x 3 in pairs 48.2, 12 x 4 in pairs
+// 50.6, 12 x 4 one at a time 52.2, 8 x 6 in threes 58.3, 20 x 2 (spills)
+// 45.2.
+using Shape8Deep = Shape8<16, 3, 1, 1>;
 // Grids of several waves with short partitions run several CTAs per SM, so
 // that one CTA's start (table and context loads, first request) and end
-// (merge, state write) overlap the others' streaming: three of 4 warps x 4
-// stages (about 70 KiB each) for partitions up to 1024 positions, two of 6
-// warps x 4 stages (about 105 KiB) up to 2048. B = 1, Hq = 32, T = 131072
-// (us, two / three CTAs per SM): 512-position partitions 76.9 / 66.3, 1024
-// 65.2 / 61.0, 2048 60.4 / 68.8.
-using Shape8Pair = Shape8<6, 4, 2>;
-using Shape8Trio = Shape8<4, 4, 3>;
+// (merge, state write) overlap the others' streaming: four of 4 warps x 3
+// stages (about 52 KiB each) for partitions up to 1024 positions, two of 8
+// warps x 3 stages (about 104 KiB) up to 2048; 16 warps per SM as above,
+// each folding one chunk at a time. B = 1, Hq = 32, T = 131072 (us, this
+// shape / the earlier three of 4 x 4 or two of 6 x 4, in pairs): 512-position
+// partitions 58.9 / 64.9, 1024 52.5 / 60.3, 2048 56.3 / 60.0; three of
+// 4 x 4 one at a time 66.0 (512) and 62.5 (1024); 512-position partitions
+// on two of 8 x 3: 67.8.
+using Shape8Pair = Shape8<8, 3, 2, 1>;
+using Shape8Quad = Shape8<4, 3, 4, 1>;
 constexpr int kPairMaxPositions8 = 2048;
-constexpr int kTrioMaxPositions8 = 1024;
+constexpr int kQuadMaxPositions8 = 1024;
 
 struct Int8Params {
     const uint16_t *q;
@@ -813,16 +821,16 @@ template <typename S> bool merges_in_kernel(int G, int num_partitions)
            static_cast<long>(G) * num_partitions * kHeadDim * 4 + S::kMergeScratch <= S::kStageArea;
 }
 
-enum class Shape8Kind { kShort, kDeep, kPair, kTrio };
+enum class Shape8Kind { kShort, kDeep, kPair, kQuad };
 
 template <int G>
 cudaError_t launch_int8_g(const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &ms,
                           const Int8Params &kp, dim3 grid, bool fused, Shape8Kind shape, cudaStream_t stream)
 {
-    if constexpr (G <= Shape8Trio::kWarps) {
-        if (shape == Shape8Kind::kTrio)
-            return fused ? launch_int8_t<G, true, Shape8Trio>(mk, mv, ms, kp, grid, stream)
-                         : launch_int8_t<G, false, Shape8Trio>(mk, mv, ms, kp, grid, stream);
+    if constexpr (G <= Shape8Quad::kWarps) {
+        if (shape == Shape8Kind::kQuad)
+            return fused ? launch_int8_t<G, true, Shape8Quad>(mk, mv, ms, kp, grid, stream)
+                         : launch_int8_t<G, false, Shape8Quad>(mk, mv, ms, kp, grid, stream);
     }
     if constexpr (G <= Shape8Pair::kWarps) {
         if (shape == Shape8Kind::kPair)
@@ -898,18 +906,18 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
         kp.freqs = make_rope_freqs(a.rope_theta);
     }
     // Grids of more than one wave (of one CTA per SM) with short partitions
-    // take three or two CTAs per SM (the fused step and attention alone
-    // alike, so they give equal bits); otherwise long partitions take 12
-    // warps x 4 stages, short ones 12 warps x 3 (both fold-bound).
+    // take four or two CTAs per SM (the fused step and attention alone
+    // alike, so they give equal bits); otherwise long partitions take 16
+    // warps x 3 stages, short ones 12 warps x 3 (both fold-bound).
     const long part_positions = static_cast<long>(a.pages_per_part) * a.page_size;
     const bool waves = a.num_partitions > 1 &&
                        static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);
     Shape8Kind shape = part_positions >= kDeepChunks8 * kChunkTokens ? Shape8Kind::kDeep : Shape8Kind::kShort;
-    if (waves && G <= Shape8Trio::kWarps && part_positions <= kTrioMaxPositions8)
-        shape = Shape8Kind::kTrio;
+    if (waves && G <= Shape8Quad::kWarps && part_positions <= kQuadMaxPositions8)
+        shape = Shape8Kind::kQuad;
     else if (waves && G <= Shape8Pair::kWarps && part_positions <= kPairMaxPositions8)
         shape = Shape8Kind::kPair;
-    const bool in_kernel = shape == Shape8Kind::kTrio   ? merges_in_kernel<Shape8Trio>(G, a.num_partitions)
+    const bool in_kernel = shape == Shape8Kind::kQuad   ? merges_in_kernel<Shape8Quad>(G, a.num_partitions)
                            : shape == Shape8Kind::kPair ? merges_in_kernel<Shape8Pair>(G, a.num_partitions)
                            : shape == Shape8Kind::kDeep ? merges_in_kernel<Shape8Deep>(G, a.num_partitions)
                                                         : merges_in_kernel<Shape8Short>(G, a.num_partitions);

@@ -97,18 +97,20 @@ def test_int8_attention_group_sizes(Hq, Hkv):
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (24, 8), (64, 8), (4, 1)])
 @pytest.mark.parametrize("num_partitions", [1, 2])
 def test_int8_attention_long_partitions(Hq, Hkv, num_partitions):
-    """Partitions of 64 chunks (1024 positions) or more run the 12-warp CTA
+    """Partitions of 64 chunks (1024 positions) or more run the 16-warp CTA
     shape; a ragged tail and every group size on it."""
     kv = inputs.paged_kv(1150 + Hq + num_partitions, [2000, 1100, 7], Hkv=Hkv, page_size=16, fill_unused="normal")
     check_attention(kv, inputs.query(1150 + Hq, 3, Hq), num_partitions)
 
 
-@pytest.mark.parametrize("Hq,num_partitions", [(16, 19), (16, 64), (64, 60)])
+@pytest.mark.parametrize("Hq,num_partitions", [(16, 19), (8, 64), (16, 64), (64, 60)])
 def test_int8_merge_paths_and_workspace_reuse(Hq, num_partitions):
     """Up to 64 partitions whose states fit the stage area are merged by the
-    last CTA (16 heads at 19 and 64); 8 heads at 60 partitions do not fit and
-    go to the merge kernel. The same workspace serves repeated calls (the
-    ticket is left at zero) with identical results."""
+    last CTA: these grids run four CTAs per SM (48 KiB of stages each), which
+    hold 2 heads' states at 19 partitions and 1 head's at 64. 2 heads at 64
+    and 8 at 60 do not fit and go to the merge kernel. The same workspace
+    serves repeated calls (the ticket is left at zero) with identical
+    results."""
     ctx = [3000, 64 * 16 + 3, 40]
     kv = inputs.paged_kv(1210 + num_partitions, ctx, Hkv=8, page_size=16, fill_unused="normal")
     q = inputs.query(1210 + num_partitions, len(ctx), Hq)

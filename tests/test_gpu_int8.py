@@ -259,12 +259,14 @@ def _fused_vs_two_launch(seed, ctx, Hq, num_partitions, page_size=16):
     ([2049, 40, 8000], 16, 0),
     ([2049, 40, 8000], 16, 70),
     ([700, 1], 64, 5),
+    ([2049, 40, 3000], 64, 24),
     ([512, 513], 8, 1),
 ])
 def test_int8_fused_step_equals_two_launches(ctx, Hq, num_partitions):
     """decode_step_paged_int8 writes the same codes and scales, the same
     rotated query and the same outputs (bit for bit) as the quantizing
-    prologue followed by the INT8 attention."""
+    prologue followed by the INT8 attention (one and several CTAs per SM:
+    70 partitions of g = 2 run four per SM, 24 of g = 8 two per SM)."""
     res, *_ = _fused_vs_two_launch(1300 + sum(ctx) % 97 + Hq, ctx, Hq, num_partitions)
     for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
         assert np.array_equal(a, b, equal_nan=False), name
@@ -288,12 +290,13 @@ def test_int8_fused_step_matches_the_oracle(num_partitions):
     assert pg.device_error_flags() == 0
 
 
-@pytest.mark.parametrize("Hq,num_partitions", [(8, 64), (24, 32), (48, 40)])
+@pytest.mark.parametrize("Hq,num_partitions", [(8, 64), (24, 28), (24, 32), (48, 40)])
 def test_int8_several_ctas_per_sm(Hq, num_partitions):
-    """Several waves of short partitions (8 sequences x 8 KV heads x 32-64
-    partitions of 32-64 positions) run several CTAs per SM: three of 4 warps
-    for g = 1 and 3, two of 6 warps for g = 6 (which merges in merge_kernel;
-    the others merge in the last CTA).
+    """Several waves of short partitions (8 sequences x 8 KV heads x 26-64
+    partitions of 32-80 positions) run several CTAs per SM: four of 4 warps
+    (48 KiB of stages each) for g = 1 and 3, two of 8 warps for g = 6. The
+    last CTA merges g = 1 at 64 partitions and g = 3 at 26 (28 asked); g = 3
+    at 32 and g = 6 at 32 (40 asked) do not fit and merge in merge_kernel.
     Attention against the oracle's INT8 attention, the fused step against the
     oracle's chain and bit for bit against the two launches."""
     ctx = [2048, 1, 2, 1500, 2047, 700, 2048, 33]

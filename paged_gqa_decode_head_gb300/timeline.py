@@ -9,11 +9,13 @@ CTAs, averaged over layers 4..27 and several replays. The stamps themselves
 cost a little: the instrumented step runs a few tenths of a microsecond
 slower per layer than the plain library, which the tool reports beside it.
 
-    python -m paged_gqa_decode_head_gb300.timeline [--replays 10] [--partitions 0] [--int8]
+    python -m paged_gqa_decode_head_gb300.timeline [--replays 10] [--partitions 0] [--int8 | --multi]
 
 --int8 runs the same chain over an INT8 cache (decode_step_paged_int8 and
 decode_attn_paged_int8; codes uniform in [-127, 127], scales 1/127, as the
-benchmark's INT8 chain).
+benchmark's INT8 chain). --multi runs the M = 4 multi-token chain
+(decode_step_paged_multi and decode_attn_paged_multi, the benchmark's
+qwen3_0p6b_t8k_m4 workload).
 """
 from __future__ import annotations
 
@@ -127,24 +129,89 @@ class Int8Chain:
                                                num_partitions=self.num_partitions)
 
     def capture(self, prologue: bool = True, fused: bool = False):
+        return _capture(lambda: self.run(fused))
+
+
+class MultiChain:
+    """The 28-layer T = 8192 chain with M = 4 new tokens per layer, with
+    DecodeStep's partitions and capture() interface (the benchmark's M = 4
+    leg). Attention alone runs on the raw queries."""
+
+    def __init__(self, num_partitions: int):
         import torch
 
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            self.run(fused)
-        torch.cuda.current_stream().wait_stream(s)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.run(fused)
-        return g
+        from . import binding, inputs
+        from .runner import to_device_bf16, to_device_i32
+
+        w = inputs.WORKLOADS["qwen3_0p6b_t8k_m4"]
+        self.w = w
+        self.num_partitions = num_partitions
+        B, M, Hq = w["B"], w["M"], w["Hq"]
+        self.bufs = []
+        for kv, q, k, v, gq, gk in inputs.qwen3_layers_multi():
+            self.bufs.append(dict(
+                kc=to_device_bf16(kv.k_cache, "cuda"), vc=to_device_bf16(kv.v_cache, "cuda"),
+                bt=to_device_i32(kv.block_table, "cuda"), ctx=to_device_i32(kv.context_lens, "cuda"),
+                q=to_device_bf16(q, "cuda"), k=to_device_bf16(k, "cuda"), v=to_device_bf16(v, "cuda"),
+                gq=to_device_bf16(gq, "cuda"), gk=to_device_bf16(gk, "cuda"),
+                q_out=torch.empty((B, M, Hq, 128), dtype=torch.bfloat16, device="cuda"),
+                out=torch.empty((B, M, Hq, 128), dtype=torch.float32, device="cuda"),
+                P=kv.page_size, mp=kv.max_pages))
+        b0 = self.bufs[0]
+        n = binding.decode_attn_multi_workspace_size(B, M, Hq, w["Hkv"], 128, b0["P"], b0["mp"], num_partitions)
+        self.ws = torch.zeros(max(16, n), dtype=torch.uint8, device="cuda")
+
+    @property
+    def partitions(self) -> int:
+        from . import binding
+
+        b0 = self.bufs[0]
+        return binding.decode_attn_partition_count(self.w["B"], self.w["Hkv"], b0["P"], b0["mp"],
+                                                   self.num_partitions)
+
+    def run(self, fused: bool):
+        import math
+
+        from . import binding
+
+        scale = 1.0 / math.sqrt(128)
+        for b_ in self.bufs:
+            if fused:
+                binding.decode_step_paged_multi(b_["q"], b_["k"], b_["v"], b_["gq"], b_["gk"], b_["ctx"], b_["bt"],
+                                                b_["kc"], b_["vc"], scale, self.w["theta"], q_out=b_["q_out"],
+                                                out_f32=b_["out"], workspace=self.ws,
+                                                num_partitions=self.num_partitions)
+            else:
+                binding.decode_attn_paged_multi(b_["q"], b_["kc"], b_["vc"], b_["bt"], b_["ctx"], scale,
+                                                out_f32=b_["out"], workspace=self.ws,
+                                                num_partitions=self.num_partitions)
+
+    def capture(self, prologue: bool = True, fused: bool = False):
+        return _capture(lambda: self.run(fused))
+
+
+def _capture(run):
+    """Warm-up run on a side stream, then the same run captured as a graph."""
+    import torch
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    return g
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--replays", type=int, default=10)
     ap.add_argument("--partitions", type=int, default=0, help="0: the library's automatic count")
-    ap.add_argument("--int8", action="store_true", help="the INT8 cache's step and attention instead of bf16")
+    mode = ap.add_mutually_exclusive_group()
+    mode.add_argument("--int8", action="store_true", help="the INT8 cache's step and attention instead of bf16")
+    mode.add_argument("--multi", action="store_true", help="the M = 4 multi-token step and attention")
     ap.add_argument("--library", default=None,
                     help="an already built timeline library (default: build libpgqa_timeline.so here)")
     args = ap.parse_args(argv)
@@ -161,18 +228,25 @@ def main(argv=None):
     slots = lib.pgqa_timeline_attach(None, 1)
     L = 28
     w = inputs.WORKLOADS["qwen3_0p6b_t8k"]
-    step = Int8Chain(L, args.partitions) if args.int8 else DecodeStep(
-        inputs.qwen3_layers(layers=L), Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"],
-        num_partitions=args.partitions)
+    if args.int8:
+        step = Int8Chain(L, args.partitions)
+    elif args.multi:
+        step = MultiChain(args.partitions)
+    else:
+        step = DecodeStep(inputs.qwen3_layers(layers=L), Hq=w["Hq"], Hkv=w["Hkv"], rope_theta=w["theta"],
+                          num_partitions=args.partitions)
     np_used = step.partitions
     grid = np_used * w["Hkv"]
     buf = torch.zeros(L * grid * slots, dtype=torch.int64, device="cuda")
-    print(f"28 layers, B=1, Hq=16, Hkv=8, T=8192, NP={np_used} ({grid} CTAs per launch)")
+    print(f"28 layers, B=1, Hq=16, Hkv=8, T=8192{', M=4' if args.multi else ''}, NP={np_used} "
+          f"({grid} CTAs per launch)")
     keep = []
     for fused in (True, False):
         name = "fused step (decode_step_paged)" if fused else "attention alone (decode_attn_paged)"
         if args.int8:
             name = name.replace("paged)", "paged_int8)")
+        if args.multi:
+            name = name.replace("paged)", "paged_multi)")
         lib.pgqa_timeline_attach(None, 1)
         plain = step.capture(prologue=fused, fused=fused)
         # the capture's warm-up run takes the first L launch slots, the

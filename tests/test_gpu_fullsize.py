@@ -116,12 +116,15 @@ def test_ragged_b64_full_size_every_sequence():
     print(f"ragged B=64: worst |out - oracle| = {err.max():.2e} over {B} sequences")
 
 
-def test_long_split_kv_t131072_np256():
+@pytest.mark.parametrize("np_req", [0, 256])
+def test_long_split_kv_t131072(np_req):
+    """Both launch forms the benchmark times: the automatic partition count
+    (one wave, 19 partitions) and the workload's 512-position partitions."""
     w = inputs.WORKLOADS["long_split_kv_t128k"]
     kv, q = inputs.long_split_kv()
     dev = "cuda"
-    np_req = w["T"] // w["partition"]
-    assert pg.decode_attn_partition_count(1, w["Hkv"], 16, kv.max_pages, np_req) == 256
+    assert np_req in (0, w["T"] // w["partition"])
+    assert pg.decode_attn_partition_count(1, w["Hkv"], 16, kv.max_pages, np_req) == (np_req or 19)
     ws = torch.zeros(pg.decode_attn_workspace_size(1, w["Hq"], w["Hkv"], 128, 16, kv.max_pages, np_req),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((1, w["Hq"], 128), dtype=torch.float32, device=dev)
@@ -160,3 +163,47 @@ def test_host_tiled_t65536(tiles_per_copy):
     torch.cuda.synchronize()
     ref = oracle.attention_contiguous(q, k, v, SCALE)
     assert np.abs(out.cpu().numpy() - ref).max() <= ATOL_F32
+
+
+def _per_kv_head_oracle(fn, q, caches, G):
+    """fn(q of one KV head's G query heads, *that head's caches) on one host
+    thread per KV head, results joined along the head axis."""
+    Hkv = caches[0].shape[1]
+
+    def one(h):
+        return fn(q[:, h * G:(h + 1) * G].copy(), *[c[:, h:h + 1].copy() for c in caches])
+
+    with concurrent.futures.ThreadPoolExecutor(min(Hkv, _host_threads())) as ex:
+        return np.concatenate(list(ex.map(one, range(Hkv))), axis=1)
+
+
+@pytest.mark.parametrize("np_req", [0, 256])
+def test_long_split_kv_t131072_int8(np_req):
+    """The INT8 attention on the long-context workload quantized by the
+    oracle, in both launch forms the benchmark times: automatic partitions
+    (one CTA of 16 warps per SM) and 512-position partitions (four CTAs per
+    SM, merged by merge_kernel)."""
+    w = inputs.WORKLOADS["long_split_kv_t128k"]
+    kv, q = inputs.long_split_kv()
+    dev = "cuda"
+    k8, ks = oracle.quantize_rows_int8(kv.k_cache)
+    v8, vs = oracle.quantize_rows_int8(kv.v_cache)
+    B, Hq, Hkv = 1, w["Hq"], w["Hkv"]
+    ws = torch.zeros(max(16, pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, 16, kv.max_pages, np_req)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    outb = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    pg.decode_attn_paged_int8(to_device_bf16(q, dev), torch.from_numpy(k8).to(dev), torch.from_numpy(v8).to(dev),
+                              torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev),
+                              to_device_i32(kv.block_table, dev), to_device_i32(kv.context_lens, dev), SCALE,
+                              out_f32=out, out_bf16=outb, workspace=ws, num_partitions=np_req)
+    torch.cuda.synchronize()
+    assert pg.device_error_flags() == 0
+    ref = _per_kv_head_oracle(
+        lambda qh, k8h, v8h, ksh, vsh: oracle.decode_attention_int8(qh, k8h, v8h, ksh, vsh, kv.block_table,
+                                                                     kv.context_lens, SCALE),
+        q, (k8, v8, ks, vs), Hq // Hkv)
+    err = np.abs(out.cpu().numpy() - ref).max()
+    assert err <= ATOL_F32
+    assert_bf16_close(bf16_bits(outb), oracle.round_bf16(ref))
+    print(f"INT8 T=131072 NP={np_req or 19}: worst |out - oracle| = {err:.2e}")

@@ -116,6 +116,42 @@ def test_ragged_b64_full_size_every_sequence():
     print(f"ragged B=64: worst |out - oracle| = {err.max():.2e} over {B} sequences")
 
 
+def test_ragged_b64_int8_full_size_every_sequence():
+    """The INT8 attention on the ragged batch's pool quantized by the oracle,
+    automatic partitions (the benchmark's launch): every sequence against the
+    oracle's INT8 attention at both bars."""
+    w = inputs.WORKLOADS["ragged_b64"]
+    kv, q = inputs.ragged_b64()
+    dev = "cuda"
+    B, Hq, Hkv = w["B"], w["Hq"], w["Hkv"]
+    k8, ks = oracle.quantize_rows_int8(kv.k_cache)
+    v8, vs = oracle.quantize_rows_int8(kv.v_cache)
+    del kv.k_cache, kv.v_cache
+    ws = torch.zeros(max(16, pg.decode_attn_int8_workspace_size(B, Hq, Hkv, 128, 16, kv.max_pages, 0)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    outb = torch.full((B, Hq, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    caches = [torch.from_numpy(a).to(dev) for a in (k8, v8, ks, vs)]
+    pg.decode_attn_paged_int8(to_device_bf16(q, dev), *caches, to_device_i32(kv.block_table, dev),
+                              to_device_i32(kv.context_lens, dev), SCALE, out_f32=out, out_bf16=outb, workspace=ws)
+    torch.cuda.synchronize()
+    assert pg.device_error_flags() == 0
+    o = out.cpu().numpy().astype(np.float64)
+    ob = bf16_bits(outb)
+    del caches
+
+    def reference(b):
+        return oracle.decode_attention_int8(q[b:b + 1], k8, v8, ks, vs, kv.block_table[b:b + 1],
+                                            kv.context_lens[b:b + 1], SCALE)
+
+    with concurrent.futures.ThreadPoolExecutor(_host_threads()) as ex:
+        ref = np.concatenate(list(ex.map(reference, range(B))))
+    err = np.abs(o - ref).max(axis=(1, 2))
+    assert (err <= ATOL_F32).all(), np.argwhere(err > ATOL_F32).ravel()
+    assert_bf16_close(ob, oracle.round_bf16(ref), "out_bf16")
+    print(f"INT8 ragged B=64: worst |out - oracle| = {err.max():.2e} over {B} sequences")
+
+
 @pytest.mark.parametrize("np_req", [0, 256])
 def test_long_split_kv_t131072(np_req):
     """Both launch forms the benchmark times: the automatic partition count

@@ -118,6 +118,7 @@ struct SplitParams {
     int Hq, Hkv, P, max_pages, num_pages, NP, ppp;
     int G, M; // group size; new tokens per sequence (column n = query n / G, head n % G)
     int fused_merge;
+    int walk; // decode_walk_kernel: partitions per CTA
     float scale_log2;
     // fused decode step only: the new token's raw heads and the prologue's
     // parameters; the kernel normalises/rotates q and appends K/V itself
@@ -876,6 +877,312 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
         *ticket = 0u; // ready for the next call
 }
 
+// Attention alone over many short partitions (more CTAs than one wave of the
+// two-CTA shape, partition states merged by merge_kernel), walked: each CTA
+// takes a run of consecutive partitions of one (sequence, KV head), and its
+// warps keep requesting the next partition's chunks while they finish the
+// current one, so no CTA start (table, context, first requests) or end
+// (records, state write) leaves an SM without bytes in flight. Within a
+// partition the chunks, their warps (chunk c of the partition: warp
+// c % kWarps), the fold pairs and the record merge are the two-CTA shape's,
+// so every partition state, and the merged outputs, equal that kernel's bit
+// for bit; decode_step_paged keeps the two-CTA shape for such grids and still
+// matches the two launches.
+// Shared memory: the stages, their mbarriers and valid-row counts, then two
+// slots of kWarps records (partitions alternate between them), their arrival
+// counts and the partition each slot is free for.
+template <int NCOL, int kS> struct WalkShape {
+    static constexpr int kWarps = PairShape::kWarps;
+    static constexpr int kStages = kS;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kBarOffset = kWarps * kStages * kStageBytes;
+    static constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
+    static constexpr int kRecFloats = (NCOL * kHeadDim + 2 * NCOL + 3) & ~3;
+    static constexpr int kRecOffset = (kRowsOffset + kWarps * kStages * 4 + 15) & ~15;
+    static constexpr int kSlotOffset = kRecOffset + 2 * kWarps * kRecFloats * 4;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kSlotOffset + 16;
+    static_assert(kSmem <= 232448, "at most 227 KB of shared memory per CTA");
+};
+// 4 stages per warp where the records leave room for them (NCOL <= 4), else 3.
+template <int NCOL> using WalkShapeFor = WalkShape<NCOL, NCOL <= 4 ? 4 : 3>;
+
+template <int NCOL, typename S>
+__global__ void __launch_bounds__(S::kThreads, 1)
+    decode_walk_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                       const SplitParams p)
+{
+    constexpr int kWarps = S::kWarps, kStages = S::kStages, kRec = S::kRecFloats;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
+
+    allow_dependent_launch();
+    unsigned char *stages = smem + warp * kStages * kStageBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset) + warp * kStages;
+    int *stage_rows = reinterpret_cast<int *>(smem + S::kRowsOffset) + warp * kStages;
+    float *recs = reinterpret_cast<float *>(smem + S::kRecOffset); // [2][kWarps][kRec]
+    int *arrivals = reinterpret_cast<int *>(smem + S::kSlotOffset); // [2]
+    volatile int *free_for = reinterpret_cast<volatile int *>(smem + S::kSlotOffset + 8); // [2]
+    if (lane == 0) {
+        if (warp == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+#pragma unroll
+        for (int s = 0; s < kStages; ++s)
+            mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+
+    const int part_tokens = p.ppp * p.P; // a multiple of the 16-position chunk (P >= 16)
+    const int cpp = part_tokens / kChunkTokens;
+    const int32_t *table = p.block_table + static_cast<size_t>(b) * p.max_pages;
+    int T = p.context_lens[b];
+    if (T < 0 || T > p.max_pages * p.P) {
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            raise_flag(PGQA_DEVERR_BAD_CONTEXT);
+        T = 0;
+    }
+    const int n_parts = max(1, (T + part_tokens - 1) / part_tokens);
+    const int j0 = blockIdx.x * p.walk;
+    const int j1 = min(n_parts, j0 + p.walk);
+    if (threadIdx.x == 0) {
+        arrivals[0] = arrivals[1] = 0;
+        free_for[j0 & 1] = j0;
+        free_for[(j0 + 1) & 1] = j0 + 1;
+    }
+    __syncthreads();
+    if (j0 >= j1) {
+        grid_dependency_wait(); // keep the chain ordered even when idle
+        return;
+    }
+
+    // This warp's chunks, partition after partition: nkf in each full
+    // partition of the run, nk_last in a last, shorter one (the sequence's
+    // end); chunk r of the walk is chunk k of partition j, position
+    // j * part_tokens + (warp + k * kWarps) * 16.
+    const auto owned = [&](int cnt) { return cnt > warp ? (cnt - 1 - warp) / kWarps + 1 : 0; };
+    const int n_full = max(0, min(j1, T / part_tokens) - j0);
+    const bool has_last = j1 - j0 > n_full;
+    const int nkf = owned(cpp);
+    const int nk_last = has_last ? owned((T - (j1 - 1) * part_tokens + kChunkTokens - 1) / kChunkTokens) : 0;
+    const int total = nkf * n_full + nk_last;
+    const auto chunk_pos = [&](int r) {
+        const int in_full = nkf * n_full;
+        const int j = r < in_full ? j0 + r / nkf : j0 + n_full;
+        const int k = r < in_full ? r % nkf : r - in_full;
+        return j * part_tokens + (warp + k * kWarps) * kChunkTokens;
+    };
+    // Physical pages of this warp's chunks, 32 at a time: lane L caches the
+    // entry of chunk 32*blk + L. Called by the whole (converged) warp.
+    int tbl_blk = -1, tbl_val = -1;
+    const auto phys_of = [&](int r) {
+        if ((r >> 5) != tbl_blk) {
+            tbl_blk = r >> 5;
+            const int rr = (tbl_blk << 5) + lane;
+            tbl_val = rr < total ? table[chunk_pos(rr) / p.P] : -1;
+        }
+        return __shfl_sync(0xFFFFFFFFu, tbl_val, r & 31);
+    };
+    // Lane 0 requests chunk r (phys from phys_of) and records its valid rows
+    // (partitions are whole chunks: only the sequence's end cuts one short).
+    const auto issue = [&](int r, int phys, uint64_t policy) {
+        const int t = chunk_pos(r);
+        uint64_t *bar = &bars[r % kStages];
+        if (phys < 0 || phys >= p.num_pages) {
+            raise_flag(PGQA_DEVERR_BAD_PAGE);
+            stage_rows[r % kStages] = 0;
+            mbar_arrive(bar); // complete the phase with no data; the keys are masked
+            return;
+        }
+        stage_rows[r % kStages] = min(kChunkTokens, T - t);
+        const int row = (phys * p.Hkv + kvh) * p.P + (t % p.P);
+        unsigned char *dst = stages + (r % kStages) * kStageBytes;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        tma_load_3d(dst, &tmap_k, 0, row, 0, bar, policy);
+        tma_load_3d(dst + 2 * kBoxBytes, &tmap_v, 0, row, 0, bar, policy);
+    };
+    // The chunk holding the new position T-1 is written by the prologue this
+    // kernel may overlap: it is requested after griddepcontrol.wait.
+    const auto holds_new_token = [&](int r) { return chunk_pos(r) + kChunkTokens > T - 1; };
+
+    const uint64_t policy = l2_evict_first_policy();
+    const int first = min(kStages, total);
+    int first_phys[kStages];
+#pragma unroll
+    for (int k = 0; k < kStages; ++k)
+        first_phys[k] = k < first ? phys_of(k) : -1;
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kStages; ++k)
+            if (k < first && !holds_new_token(k))
+                issue(k, first_phys[k], policy);
+    }
+    grid_dependency_wait();
+    MmaWarp<NCOL> st;
+    const int col = lane >> 2; // this lane's B-operand column
+    st.init(col < NCOL ? p.q + column_row<false>(p, b, kvh, col) * kHeadDim : nullptr);
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < kStages; ++k)
+            if (k < first && holds_new_token(k))
+                issue(k, first_phys[k], policy);
+    }
+    __syncwarp();
+
+    bool ok = true;
+    int r = 0;      // next chunk of the walk to fold
+    int issued = first;
+    for (int j = j0; j < j1 && ok; ++j) {
+        const int nk = j - j0 < n_full ? nkf : nk_last;
+        // the partition's chunks in pairs, as the two-CTA shape folds them
+        for (int k0 = 0, nc; k0 < nk; k0 += nc) {
+            nc = min(2, nk - k0);
+            uint32_t stage_addr[2];
+            int lim[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int rr = r + c;
+                stage_addr[c] = smem_addr(stages + (rr % kStages) * kStageBytes);
+                lim[c] = 0;
+                if (c < nc) {
+                    const bool landed = mbar_wait_bounded(&bars[rr % kStages], (rr / kStages) & 1);
+                    if (!__all_sync(0xFFFFFFFFu, landed))
+                        ok = false;
+                    lim[c] = stage_rows[rr % kStages];
+                    if (lim[c] < kChunkTokens) {
+                        // rows past the history may hold anything, even NaN:
+                        // zero their V so that p = 0 times V stays 0
+                        unsigned char *stage = stages + (rr % kStages) * kStageBytes;
+                        const int n_units = (kChunkTokens - lim[c]) * 16;
+                        for (int u = lane; u < n_units; u += 32) {
+                            const int row = lim[c] + u / 16;
+                            const int box = 2 + ((u >> 3) & 1);
+                            *reinterpret_cast<uint4 *>(stage + box * kBoxBytes + row * 128 + (u & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        __syncwarp();
+                    }
+                }
+            }
+            if (!ok)
+                break;
+            if (nc == 2)
+                st.template fold<2, false>(stage_addr, lim, lim, p.scale_log2);
+            else
+                st.template fold<1, false>(stage_addr, lim, lim, p.scale_log2);
+            __syncwarp();
+            // the folded stages take the walk's next chunks, whatever their partition
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int rn = r + c + kStages;
+                if (c < nc && rn < total) {
+                    const int phys = phys_of(rn);
+                    if (lane == 0) {
+                        fence_proxy_async_smem();
+                        issue(rn, phys, policy);
+                    }
+                    issued = rn + 1;
+                }
+            }
+            r += nc;
+        }
+        if (!ok)
+            break;
+        // This warp's record of partition j into slot j % 2, once the
+        // partition that used the slot before (j - 2) has been merged.
+        const int s = j & 1;
+        if (lane == 0) {
+            const unsigned long long t0 = globaltimer_ns();
+            while (free_for[s] != j) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        if (lane == 0)
+            __threadfence_block(); // the slot's reset arrival count before this warp's arrival
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok)
+            break;
+        float *slot = recs + s * kWarps * kRec;
+        st.store_record(slot + warp * kRec);
+        st.clear();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&arrivals[s], 1) == kWarps - 1;
+            __threadfence_block();
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, last, 0))
+            continue;
+        __syncwarp();
+        // The last warp to arrive merges the partition's kWarps records with
+        // the operations, in the order, of the CTA-wide merge of the
+        // two-CTA shape, four dims per lane.
+        const int d = 4 * lane;
+#pragma unroll 1
+        for (int h = 0; h < NCOL; ++h) {
+            float M = kEmptyMax;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                M = fmaxf(M, slot[w * kRec + NCOL * kHeadDim + h]);
+            float L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float wt = exp2f(slot[w * kRec + NCOL * kHeadDim + h] - M);
+                L = fmaf(slot[w * kRec + NCOL * kHeadDim + NCOL + h], wt, L);
+                const float4 v = *reinterpret_cast<const float4 *>(slot + w * kRec + h * kHeadDim + d);
+                O[0] = fmaf(v.x, wt, O[0]);
+                O[1] = fmaf(v.y, wt, O[1]);
+                O[2] = fmaf(v.z, wt, O[2]);
+                O[3] = fmaf(v.w, wt, O[3]);
+            }
+            const size_t row = column_row<false>(p, b, kvh, h);
+            if (n_parts == 1) {
+                float o[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    o[i] = L > 0.f ? O[i] / L : 0.f;
+                if (p.out_f32)
+                    *reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
+                if (p.out_bf16)
+                    *reinterpret_cast<uint2 *>(p.out_bf16 + row * kHeadDim + d) =
+                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+            } else {
+                const size_t idx = row * p.NP + j;
+                if (lane == 0) {
+                    p.ws_m[idx] = M; // base-2 units (private workspace format)
+                    p.ws_l[idx] = L;
+                }
+                *reinterpret_cast<float4 *>(p.ws_acc + idx * kHeadDim + d) = make_float4(O[0], O[1], O[2], O[3]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            arrivals[s] = 0;
+            __threadfence_block();
+            free_for[s] = j + 2;
+        }
+        __syncwarp();
+    }
+    if (!ok) {
+        // A copy or a record slot never became ready: flag it and wait
+        // (bounded) for the copies still in flight into this warp's stages.
+        if (lane == 0)
+            raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
+        for (int rr = r; rr < issued; ++rr)
+            (void)mbar_wait_bounded(&bars[rr % kStages], (rr / kStages) & 1);
+    }
+}
+
 struct MergeParams {
     const float *m, *l, *acc;
     int Hq, NP;
@@ -1041,6 +1348,45 @@ cudaError_t launch_split(const CUtensorMap &mk, const CUtensorMap &mv, const Spl
     }
     return fused ? launch_split_t<NCOL, true, false, SoloShape>(mk, mv, kp, grid, stream)
                  : launch_split_t<NCOL, false, false, SoloShape>(mk, mv, kp, grid, stream);
+}
+
+template <int NCOL>
+cudaError_t launch_walk(const CUtensorMap &mk, const CUtensorMap &mv, const SplitParams &kp, dim3 grid,
+                        cudaStream_t stream)
+{
+    using S = WalkShapeFor<NCOL>;
+    static bool configured[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev >= kMaxDevices || !configured[dev]) {
+        err = cudaFuncSetAttribute(decode_walk_kernel<NCOL, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+        if (err != cudaSuccess)
+            return err;
+        if (dev < kMaxDevices)
+            configured[dev] = true;
+    }
+    return launch_pdl(decode_walk_kernel<NCOL, S>, grid, dim3(S::kThreads), S::kSmem, stream, mk, mv, kp);
+}
+
+// Partitions per CTA of the walked grid, or 0 when walking does not apply:
+// attention alone over a grid the two-CTA shape would run in several waves,
+// merged by merge_kernel, with few enough (sequence, KV head) pairs that
+// whole runs of partitions fill the SMs (at least 7/8 of them, one CTA each).
+int walk_partitions(bool pair, bool fused_merge, bool fused, int B, int Hkv, int num_partitions, int sm_count)
+{
+    if (!pair || fused_merge || fused)
+        return 0;
+    const long heads = static_cast<long>(B) * Hkv;
+    const long slots = sm_count > 0 ? sm_count : 1;
+    if (heads > slots)
+        return 0;
+    const long per_head = slots / heads;
+    if (per_head * heads * 8 < slots * 7)
+        return 0;
+    const int walk = static_cast<int>((num_partitions + per_head - 1) / per_head);
+    return walk >= 2 ? walk : 0;
 }
 
 // The two-CTA shape takes single-token grids of more than one wave (of one
@@ -1211,9 +1557,22 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
         kp.ws_l = reinterpret_cast<float *>(ws + align256(n * sizeof(float)));
         kp.ws_acc = reinterpret_cast<float *>(ws + 2 * align256(n * sizeof(float)));
     }
-    const dim3 grid(a.num_partitions, a.Hkv, a.B);
+    dim3 grid(a.num_partitions, a.Hkv, a.B);
     kp.G = G;
     kp.M = M;
+    kp.walk = walk_partitions(pair, kp.fused_merge != 0, a.fused, a.B, a.Hkv, a.num_partitions, a.sm_count);
+    if (kp.walk) {
+        grid.x = (a.num_partitions + kp.walk - 1) / kp.walk;
+        switch (NCOL) { // pair: NCOL <= the two-CTA shape's 6 warps
+        case 1: err = launch_walk<1>(mk, mv, kp, grid, stream); break;
+        case 2: err = launch_walk<2>(mk, mv, kp, grid, stream); break;
+        case 3: err = launch_walk<3>(mk, mv, kp, grid, stream); break;
+        case 4: err = launch_walk<4>(mk, mv, kp, grid, stream); break;
+        case 5: err = launch_walk<5>(mk, mv, kp, grid, stream); break;
+        case 6: err = launch_walk<6>(mk, mv, kp, grid, stream); break;
+        default: return cudaErrorInvalidValue;
+        }
+    } else {
     switch (NCOL) {
     case 1: err = launch_split<1>(mk, mv, kp, grid, a.fused, pair, stream); break;
     case 2: err = launch_split<2>(mk, mv, kp, grid, a.fused, pair, stream); break;
@@ -1224,6 +1583,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     case 7: err = launch_split<7>(mk, mv, kp, grid, a.fused, pair, stream); break;
     case 8: err = launch_split<8>(mk, mv, kp, grid, a.fused, pair, stream); break;
     default: return cudaErrorInvalidValue;
+    }
     }
     if (err != cudaSuccess || a.num_partitions <= 1 || kp.fused_merge)
         return err;

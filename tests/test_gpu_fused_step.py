@@ -130,6 +130,47 @@ def test_fused_step_matches_the_two_launches_bit_for_bit(num_partitions):
     assert np.array_equal(fused["of"], two["of"])
 
 
+def walked(B, Hq, Hkv, P, max_pages, num_partitions):
+    """The library's rule for walking partitions (decode_walk_kernel): attention
+    alone over a grid of the two-CTA shape (one new token, g <= 6, more CTAs
+    than SMs, partitions of at most 2048 positions) whose states the merge
+    kernel merges (over 64 partitions, or more accumulators than its 96 KiB of
+    stages hold beside 5184 bytes of scratch), with few enough (sequence, KV
+    head) pairs that runs of partitions fill at least 7/8 of the SMs."""
+    np_used = pg.decode_attn_partition_count(B, Hkv, P, max_pages, num_partitions)
+    ppp = -(-max_pages // np_used)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = Hq // Hkv
+    pair = G <= 6 and np_used > 1 and ppp * P <= 2048 and B * Hkv * np_used > sms
+    merge_kernel = np_used > 64 or G * np_used * 128 * 4 + 5184 > 6 * 2 * 8192
+    heads = B * Hkv
+    per_head = sms // heads
+    return (pair and merge_kernel and heads <= sms and per_head * heads * 8 >= sms * 7
+            and -(-np_used // max(1, per_head)) >= 2)
+
+
+@pytest.mark.parametrize("Hq,ctx,num_partitions", [
+    (8, [5000, 129, 1], 100),       # g = 1 (79 partitions); a one-partition sequence writes its output
+    (48, [3000, 40, 700], 40),      # g = 6: accumulators too large for the in-kernel merge
+    (32, [6000, 16, 2047], 200),    # one-page partitions: 4 of 6 warps own no chunk
+    (16, [20000], 100),             # one sequence: 19 CTAs per KV head
+])
+def test_walked_partitions_equal_the_two_cta_shape(Hq, ctx, num_partitions):
+    """Attention alone over these grids walks runs of partitions per CTA;
+    the fused step keeps the two-CTA shape, one partition per CTA. Every
+    partition is folded by the same warps in the same pairs and merged in
+    the same order, so the two agree bit for bit, and both with the oracle."""
+    kv = inputs.paged_kv(370 + Hq + len(ctx), ctx, Hkv=8, page_size=16)
+    assert walked(len(ctx), Hq, 8, 16, kv.max_pages, num_partitions)
+    tok = inputs.new_token(370 + Hq, len(ctx), Hq, 8)
+    fused = check_fused(kv, tok, num_partitions)
+    two = run_unfused(kv, tok, num_partitions)
+    for key in ("q_out", "kc", "vc", "ob"):
+        assert np.array_equal(fused[key], two[key]), key
+    assert np.array_equal(fused["of"], two["of"])
+    assert pg.device_error_flags() == 0
+
+
 @pytest.mark.parametrize("Hq", [8, 24, 48])
 def test_fused_step_two_cta_shape(Hq):
     # several waves of short partitions (8 sequences x 8 KV heads x 40

@@ -337,6 +337,121 @@ template <int NCOL> struct MmaWarp {
     }
 };
 
+// With more (column, dim) elements than threads, each column's maximum,
+// weights and sum are formed once (one thread per column) instead of for every
+// element, with the same operations in the same order (M = 4 fused step, 8
+// columns: 11.04 -> 10.91 us per layer), and a thread folds four dims.
+template <int NCOL, int kWarps> constexpr bool kSharesWeights = NCOL * kHeadDim > kWarps * 32;
+
+// Folds the kWarps records of one partition -- warp w's at rec0 + w *
+// rec_stride bytes: [NCOL][128] O, then [NCOL] m, then [NCOL] l -- into the
+// partition's (m, l, acc) state, or into the outputs when it is the
+// sequence's only partition, with weights 2^(m_w - M) against the largest M.
+// wts holds [NCOL][kWarps] weights, then M [NCOL], L [NCOL] when the weights
+// are shared. Called by all kWarps * 32 threads of the CTA once every record
+// is visible to all of them.
+template <int NCOL, int kWarps, bool kMulti>
+__device__ __forceinline__ void fold_records(const SplitParams &p, const unsigned char *rec0, int rec_stride,
+                                             float *wts, int b, int kvh, int part, int n_parts)
+{
+    constexpr bool kSharedWeights = kSharesWeights<NCOL, kWarps>;
+    if constexpr (kSharedWeights) {
+        if (threadIdx.x < NCOL) {
+            const int h = threadIdx.x;
+            float M = kEmptyMax;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *rec = reinterpret_cast<const float *>(rec0 + w * rec_stride);
+                M = fmaxf(M, rec[NCOL * kHeadDim + h]);
+            }
+            float L = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *rec = reinterpret_cast<const float *>(rec0 + w * rec_stride);
+                const float wt = exp2f(rec[NCOL * kHeadDim + h] - M);
+                L = fmaf(rec[NCOL * kHeadDim + NCOL + h], wt, L);
+                wts[h * kWarps + w] = wt;
+            }
+            wts[NCOL * kWarps + h] = M;
+            wts[NCOL * kWarps + NCOL + h] = L;
+        }
+        __syncthreads();
+    }
+    // The CTA's state of column h, dims d .. d + cnt - 1: the outputs when it
+    // is the sequence's only partition, else its partition state.
+    const auto put_state = [&](int h, int d, float M, float L, const float *O, auto cnt) {
+        constexpr int kCnt = decltype(cnt)::value;
+        const size_t row = column_row<kMulti>(p, b, kvh, h);
+        if (n_parts == 1) {
+            float o[kCnt];
+#pragma unroll
+            for (int i = 0; i < kCnt; ++i)
+                o[i] = L > 0.f ? O[i] / L : 0.f;
+            if constexpr (kCnt == 4) {
+                if (p.out_f32)
+                    *reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
+                if (p.out_bf16)
+                    *reinterpret_cast<uint2 *>(p.out_bf16 + row * kHeadDim + d) =
+                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+            } else {
+                if (p.out_f32)
+                    p.out_f32[row * kHeadDim + d] = o[0];
+                if (p.out_bf16)
+                    p.out_bf16[row * kHeadDim + d] = f32_to_bf16_bits(o[0]);
+            }
+        } else {
+            const size_t idx = row * p.NP + part;
+            if (d == 0) {
+                p.ws_m[idx] = M; // base-2 units (private workspace format)
+                p.ws_l[idx] = L;
+            }
+            if constexpr (kCnt == 4)
+                *reinterpret_cast<float4 *>(p.ws_acc + idx * kHeadDim + d) = make_float4(O[0], O[1], O[2], O[3]);
+            else
+                p.ws_acc[idx * kHeadDim + d] = O[0];
+        }
+    };
+    if constexpr (kSharedWeights) {
+        // four consecutive dims per thread
+        for (int e = threadIdx.x; e < NCOL * (kHeadDim / 4); e += kWarps * 32) {
+            const int h = e / (kHeadDim / 4);
+            const int d = 4 * (e % (kHeadDim / 4));
+            float O[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float4 r =
+                    *reinterpret_cast<const float4 *>(rec0 + w * rec_stride + (h * kHeadDim + d) * 4);
+                const float wt = wts[h * kWarps + w];
+                O[0] = fmaf(r.x, wt, O[0]);
+                O[1] = fmaf(r.y, wt, O[1]);
+                O[2] = fmaf(r.z, wt, O[2]);
+                O[3] = fmaf(r.w, wt, O[3]);
+            }
+            put_state(h, d, wts[NCOL * kWarps + h], wts[NCOL * kWarps + NCOL + h], O,
+                      std::integral_constant<int, 4>{});
+        }
+    } else {
+        for (int e = threadIdx.x; e < NCOL * kHeadDim; e += kWarps * 32) {
+            const int h = e / kHeadDim;
+            const int d = e % kHeadDim;
+            float M = kEmptyMax, L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *rec = reinterpret_cast<const float *>(rec0 + w * rec_stride);
+                M = fmaxf(M, rec[NCOL * kHeadDim + h]);
+            }
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float *rec = reinterpret_cast<const float *>(rec0 + w * rec_stride);
+                const float wt = exp2f(rec[NCOL * kHeadDim + h] - M);
+                L = fmaf(rec[NCOL * kHeadDim + NCOL + h], wt, L);
+                O = fmaf(rec[h * kHeadDim + d], wt, O);
+            }
+            put_state(h, d, M, L, &O, std::integral_constant<int, 1>{});
+        }
+    }
+}
+
 // The last CTA of a (sequence, KV head) to finish merges the n (2..64)
 // partition states of its columns (partition_merge.cuh).
 template <int NCOL, bool kMulti, int kThreads>
@@ -744,111 +859,14 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     __syncthreads();
     TL_STAMP(7);
 
-    // With more (column, dim) elements than threads, each column's maximum,
-    // weights 2^(m_w - M) and sum L are formed once (one thread per column)
-    // instead of for every element: the same operations in the same order
-    // (M = 4 fused step, 8 columns: 11.04 -> 10.91 us per layer).
-    constexpr bool kSharedWeights = NCOL * kHeadDim > kWarps * 32;
     constexpr int kWeightsOffset = 8192; // in warp 0's stages, past its record
-    static_assert(!kSharedWeights || (NCOL * kHeadDim + 2 * NCOL) * 4 <= kWeightsOffset, "record overlaps weights");
-    static_assert(!kSharedWeights || kWeightsOffset + (NCOL * kWarps + 2 * NCOL) * 4 <= kStages * kStageBytes,
+    static_assert(!kSharesWeights<NCOL, kWarps> || (NCOL * kHeadDim + 2 * NCOL) * 4 <= kWeightsOffset,
+                  "record overlaps weights");
+    static_assert(!kSharesWeights<NCOL, kWarps> ||
+                      kWeightsOffset + (NCOL * kWarps + 2 * NCOL) * 4 <= kStages * kStageBytes,
                   "weights past warp 0's stages");
-    float *wts = reinterpret_cast<float *>(smem + kWeightsOffset); // [NCOL][kWarps], M [NCOL], L [NCOL]
-    if constexpr (kSharedWeights) {
-        if (threadIdx.x < NCOL) {
-            const int h = threadIdx.x;
-            float M = kEmptyMax;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-                M = fmaxf(M, rec[NCOL * kHeadDim + h]);
-            }
-            float L = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-                const float wt = exp2f(rec[NCOL * kHeadDim + h] - M);
-                L = fmaf(rec[NCOL * kHeadDim + NCOL + h], wt, L);
-                wts[h * kWarps + w] = wt;
-            }
-            wts[NCOL * kWarps + h] = M;
-            wts[NCOL * kWarps + NCOL + h] = L;
-        }
-        __syncthreads();
-    }
-    // The CTA's state of column h, dims d .. d + cnt - 1: the outputs when it
-    // is the sequence's only partition, else its partition state.
-    const auto put_state = [&](int h, int d, float M, float L, const float *O, auto cnt) {
-        constexpr int kCnt = decltype(cnt)::value;
-        const size_t row = column_row<kMulti>(p, b, kvh, h);
-        if (n_parts == 1) {
-            float o[kCnt];
-#pragma unroll
-            for (int i = 0; i < kCnt; ++i)
-                o[i] = L > 0.f ? O[i] / L : 0.f;
-            if constexpr (kCnt == 4) {
-                if (p.out_f32)
-                    *reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
-                if (p.out_bf16)
-                    *reinterpret_cast<uint2 *>(p.out_bf16 + row * kHeadDim + d) =
-                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
-            } else {
-                if (p.out_f32)
-                    p.out_f32[row * kHeadDim + d] = o[0];
-                if (p.out_bf16)
-                    p.out_bf16[row * kHeadDim + d] = f32_to_bf16_bits(o[0]);
-            }
-        } else {
-            const size_t idx = row * p.NP + part;
-            if (d == 0) {
-                p.ws_m[idx] = M; // base-2 units (private workspace format)
-                p.ws_l[idx] = L;
-            }
-            if constexpr (kCnt == 4)
-                *reinterpret_cast<float4 *>(p.ws_acc + idx * kHeadDim + d) = make_float4(O[0], O[1], O[2], O[3]);
-            else
-                p.ws_acc[idx * kHeadDim + d] = O[0];
-        }
-    };
-    if constexpr (kSharedWeights) {
-        // four consecutive dims per thread
-        for (int e = threadIdx.x; e < NCOL * (kHeadDim / 4); e += kWarps * 32) {
-            const int h = e / (kHeadDim / 4);
-            const int d = 4 * (e % (kHeadDim / 4));
-            float O[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float4 r =
-                    *reinterpret_cast<const float4 *>(smem + w * kStages * kStageBytes + (h * kHeadDim + d) * 4);
-                const float wt = wts[h * kWarps + w];
-                O[0] = fmaf(r.x, wt, O[0]);
-                O[1] = fmaf(r.y, wt, O[1]);
-                O[2] = fmaf(r.z, wt, O[2]);
-                O[3] = fmaf(r.w, wt, O[3]);
-            }
-            put_state(h, d, wts[NCOL * kWarps + h], wts[NCOL * kWarps + NCOL + h], O,
-                      std::integral_constant<int, 4>{});
-        }
-    } else {
-        for (int e = threadIdx.x; e < NCOL * kHeadDim; e += kWarps * 32) {
-            const int h = e / kHeadDim;
-            const int d = e % kHeadDim;
-            float M = kEmptyMax, L = 0.f, O = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-                M = fmaxf(M, rec[NCOL * kHeadDim + h]);
-            }
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float *rec = reinterpret_cast<const float *>(smem + w * kStages * kStageBytes);
-                const float wt = exp2f(rec[NCOL * kHeadDim + h] - M);
-                L = fmaf(rec[NCOL * kHeadDim + NCOL + h], wt, L);
-                O = fmaf(rec[h * kHeadDim + d], wt, O);
-            }
-            put_state(h, d, M, L, &O, std::integral_constant<int, 1>{});
-        }
-    }
+    fold_records<NCOL, kWarps, kMulti>(p, smem, kStages * kStageBytes, reinterpret_cast<float *>(smem + kWeightsOffset),
+                                       b, kvh, part, n_parts);
     if (n_parts == 1 || !p.fused_merge)
         return;
 
@@ -884,30 +902,39 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
 // current one, so no CTA start (table, context, first requests) or end
 // (records, state write) leaves an SM without bytes in flight. Within a
 // partition the chunks, their warps (chunk c of the partition: warp
-// c % kWarps), the fold pairs and the record merge are the two-CTA shape's,
+// c % kWarps), the fold pairs and the record fold are the two-CTA shape's,
 // so every partition state, and the merged outputs, equal that kernel's bit
 // for bit; decode_step_paged keeps the two-CTA shape for such grids and still
 // matches the two launches.
-// Shared memory: the stages, their mbarriers and valid-row counts, then two
-// slots of kWarps records (partitions alternate between them), their arrival
-// counts and the partition each slot is free for.
-template <int NCOL, int kS> struct WalkShape {
+// Shared memory: the stages, their mbarriers and valid-row counts, the
+// warps' records of the current partition, the record fold's weights and an
+// abort flag.
+template <int NCOL, int kS, int kCtas> struct WalkShape {
     static constexpr int kWarps = PairShape::kWarps;
     static constexpr int kStages = kS;
+    static constexpr int kCtasPerSm = kCtas;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kBarOffset = kWarps * kStages * kStageBytes;
     static constexpr int kRowsOffset = kBarOffset + kWarps * kStages * 8;
     static constexpr int kRecFloats = (NCOL * kHeadDim + 2 * NCOL + 3) & ~3;
     static constexpr int kRecOffset = (kRowsOffset + kWarps * kStages * 4 + 15) & ~15;
-    static constexpr int kSlotOffset = kRecOffset + 2 * kWarps * kRecFloats * 4;
-    static constexpr int kSmem = 1024 /* alignment slack */ + kSlotOffset + 16;
+    static constexpr int kWtsOffset = kRecOffset + kWarps * kRecFloats * 4;
+    static constexpr int kAbortOffset = kWtsOffset + (NCOL * kWarps + 2 * NCOL) * 4;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kAbortOffset + 16;
     static_assert(kSmem <= 232448, "at most 227 KB of shared memory per CTA");
+    static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
 };
-// 4 stages per warp where the records leave room for them (NCOL <= 4), else 3.
-template <int NCOL> using WalkShapeFor = WalkShape<NCOL, NCOL <= 4 ? 4 : 3>;
+// Two CTAs per SM of 2 stages per warp where their records leave room
+// (NCOL <= 4), else one CTA of 3 stages.
+template <int NCOL>
+using WalkShapeFor = std::conditional_t<NCOL <= 4, WalkShape<NCOL, 2, 2>, WalkShape<NCOL, 3, 1>>;
+constexpr int walk_ctas_per_sm(int ncol)
+{
+    return ncol <= 4 ? WalkShapeFor<1>::kCtasPerSm : WalkShapeFor<6>::kCtasPerSm;
+}
 
 template <int NCOL, typename S>
-__global__ void __launch_bounds__(S::kThreads, 1)
+__global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     decode_walk_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                        const SplitParams p)
 {
@@ -924,9 +951,8 @@ __global__ void __launch_bounds__(S::kThreads, 1)
     unsigned char *stages = smem + warp * kStages * kStageBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset) + warp * kStages;
     int *stage_rows = reinterpret_cast<int *>(smem + S::kRowsOffset) + warp * kStages;
-    float *recs = reinterpret_cast<float *>(smem + S::kRecOffset); // [2][kWarps][kRec]
-    int *arrivals = reinterpret_cast<int *>(smem + S::kSlotOffset); // [2]
-    volatile int *free_for = reinterpret_cast<volatile int *>(smem + S::kSlotOffset + 8); // [2]
+    float *recs = reinterpret_cast<float *>(smem + S::kRecOffset); // [kWarps][kRec]
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kAbortOffset);
     if (lane == 0) {
         if (warp == 0) {
             prefetch_tensormap(&tmap_k);
@@ -950,11 +976,8 @@ __global__ void __launch_bounds__(S::kThreads, 1)
     const int n_parts = max(1, (T + part_tokens - 1) / part_tokens);
     const int j0 = blockIdx.x * p.walk;
     const int j1 = min(n_parts, j0 + p.walk);
-    if (threadIdx.x == 0) {
-        arrivals[0] = arrivals[1] = 0;
-        free_for[j0 & 1] = j0;
-        free_for[(j0 + 1) & 1] = j0 + 1;
-    }
+    if (threadIdx.x == 0)
+        *abort = 0;
     __syncthreads();
     if (j0 >= j1) {
         grid_dependency_wait(); // keep the chain ordered even when idle
@@ -1035,12 +1058,12 @@ __global__ void __launch_bounds__(S::kThreads, 1)
     __syncwarp();
 
     bool ok = true;
-    int r = 0;      // next chunk of the walk to fold
+    int r = 0; // next chunk of the walk to fold
     int issued = first;
-    for (int j = j0; j < j1 && ok; ++j) {
+    for (int j = j0; j < j1; ++j) {
         const int nk = j - j0 < n_full ? nkf : nk_last;
         // the partition's chunks in pairs, as the two-CTA shape folds them
-        for (int k0 = 0, nc; k0 < nk; k0 += nc) {
+        for (int k0 = 0, nc; ok && k0 < nk; k0 += nc) {
             nc = min(2, nk - k0);
             uint32_t stage_addr[2];
             int lim[2];
@@ -1091,91 +1114,22 @@ __global__ void __launch_bounds__(S::kThreads, 1)
             }
             r += nc;
         }
-        if (!ok)
-            break;
-        // This warp's record of partition j into slot j % 2, once the
-        // partition that used the slot before (j - 2) has been merged.
-        const int s = j & 1;
-        if (lane == 0) {
-            const unsigned long long t0 = globaltimer_ns();
-            while (free_for[s] != j) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        if (lane == 0)
-            __threadfence_block(); // the slot's reset arrival count before this warp's arrival
-        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok)
-            break;
-        float *slot = recs + s * kWarps * kRec;
-        st.store_record(slot + warp * kRec);
+        if (!ok && lane == 0)
+            *abort = 1;
+        // The partition's records, folded as the two-CTA shape folds them;
+        // every warp's next chunks are in flight meanwhile.
+        st.store_record(recs + warp * kRec);
         st.clear();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(&arrivals[s], 1) == kWarps - 1;
-            __threadfence_block();
-        }
-        if (!__shfl_sync(0xFFFFFFFFu, last, 0))
-            continue;
-        __syncwarp();
-        // The last warp to arrive merges the partition's kWarps records with
-        // the operations, in the order, of the CTA-wide merge of the
-        // two-CTA shape, four dims per lane.
-        const int d = 4 * lane;
-#pragma unroll 1
-        for (int h = 0; h < NCOL; ++h) {
-            float M = kEmptyMax;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w)
-                M = fmaxf(M, slot[w * kRec + NCOL * kHeadDim + h]);
-            float L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float wt = exp2f(slot[w * kRec + NCOL * kHeadDim + h] - M);
-                L = fmaf(slot[w * kRec + NCOL * kHeadDim + NCOL + h], wt, L);
-                const float4 v = *reinterpret_cast<const float4 *>(slot + w * kRec + h * kHeadDim + d);
-                O[0] = fmaf(v.x, wt, O[0]);
-                O[1] = fmaf(v.y, wt, O[1]);
-                O[2] = fmaf(v.z, wt, O[2]);
-                O[3] = fmaf(v.w, wt, O[3]);
-            }
-            const size_t row = column_row<false>(p, b, kvh, h);
-            if (n_parts == 1) {
-                float o[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    o[i] = L > 0.f ? O[i] / L : 0.f;
-                if (p.out_f32)
-                    *reinterpret_cast<float4 *>(p.out_f32 + row * kHeadDim + d) = make_float4(o[0], o[1], o[2], o[3]);
-                if (p.out_bf16)
-                    *reinterpret_cast<uint2 *>(p.out_bf16 + row * kHeadDim + d) =
-                        make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
-            } else {
-                const size_t idx = row * p.NP + j;
-                if (lane == 0) {
-                    p.ws_m[idx] = M; // base-2 units (private workspace format)
-                    p.ws_l[idx] = L;
-                }
-                *reinterpret_cast<float4 *>(p.ws_acc + idx * kHeadDim + d) = make_float4(O[0], O[1], O[2], O[3]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            arrivals[s] = 0;
-            __threadfence_block();
-            free_for[s] = j + 2;
-        }
-        __syncwarp();
+        __syncthreads();
+        if (*abort)
+            break; // every thread sees the same flag after the barrier
+        fold_records<NCOL, kWarps, false>(p, reinterpret_cast<const unsigned char *>(recs), kRec * 4,
+                                          reinterpret_cast<float *>(smem + S::kWtsOffset), b, kvh, j, n_parts);
+        __syncthreads();
     }
-    if (!ok) {
-        // A copy or a record slot never became ready: flag it and wait
-        // (bounded) for the copies still in flight into this warp's stages.
+    if (*abort) {
+        // A copy never landed: flag it and wait (bounded) for the copies
+        // still in flight into this warp's stages.
         if (lane == 0)
             raise_flag(PGQA_DEVERR_WAIT_TIMEOUT);
         for (int rr = r; rr < issued; ++rr)
@@ -1193,15 +1147,16 @@ struct MergeParams {
     int P, ppp, max_pages;
 };
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeRound = 8; // partitions per warp whose loads are in flight together
+constexpr int kMergeRound = 16; // partitions per warp whose loads are in flight together
 
-// One CTA per (sequence, query head). Warp w folds partitions w, w+8, ...,
+// One CTA per (sequence, query head). Warp w folds partitions w, w+16, ...,
 // kMergeRound at a time: all loads of a round are issued before any is used,
 // and the round is folded into the warp's running (M, L, O) like the online
-// softmax update (lane i owns dims 4i..4i+3). The 8 warps' states are then
-// merged through shared memory.
+// softmax update (lane i owns dims 4i..4i+3); up to 256 partitions take one
+// round trip to memory. The 16 warps' states are then merged through shared
+// memory.
 template <bool kBase2>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p)
 {
@@ -1374,12 +1329,13 @@ cudaError_t launch_walk(const CUtensorMap &mk, const CUtensorMap &mv, const Spli
 // attention alone over a grid the two-CTA shape would run in several waves,
 // merged by merge_kernel, with few enough (sequence, KV head) pairs that
 // whole runs of partitions fill the SMs (at least 7/8 of them, one CTA each).
-int walk_partitions(bool pair, bool fused_merge, bool fused, int B, int Hkv, int num_partitions, int sm_count)
+int walk_partitions(bool pair, bool fused_merge, bool fused, int NCOL, int B, int Hkv, int num_partitions,
+                    int sm_count)
 {
     if (!pair || fused_merge || fused)
         return 0;
     const long heads = static_cast<long>(B) * Hkv;
-    const long slots = sm_count > 0 ? sm_count : 1;
+    const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * walk_ctas_per_sm(NCOL);
     if (heads > slots)
         return 0;
     const long per_head = slots / heads;
@@ -1560,7 +1516,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     dim3 grid(a.num_partitions, a.Hkv, a.B);
     kp.G = G;
     kp.M = M;
-    kp.walk = walk_partitions(pair, kp.fused_merge != 0, a.fused, a.B, a.Hkv, a.num_partitions, a.sm_count);
+    kp.walk = walk_partitions(pair, kp.fused_merge != 0, a.fused, NCOL, a.B, a.Hkv, a.num_partitions, a.sm_count);
     if (kp.walk) {
         grid.x = (a.num_partitions + kp.walk - 1) / kp.walk;
         switch (NCOL) { // pair: NCOL <= the two-CTA shape's 6 warps

@@ -176,7 +176,10 @@ size_t decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, 
  * summation order depend only on them and on the device's SM count. Up to
  * 64 partitions whose states fit the CTA's shared memory are merged by the
  * last CTA of each (sequence, KV head); otherwise a merge kernel follows in
- * the same stream.
+ * the same stream. Grids of the two-CTA shape merged that way with few
+ * (sequence, KV head) pairs run each CTA over a run of consecutive
+ * partitions; the partition states, and so the results, are those of the
+ * two-CTA shape, bit for bit.
  */
 int decode_attn_paged(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const pgqa_bf16 *v_cache,
                       const int32_t *block_table, const int32_t *context_lens, int B, int Hq,
@@ -289,7 +292,7 @@ int decode_attn_paged_multi(const pgqa_bf16 *q, const pgqa_bf16 *k_cache, const 
  *   partitions whose states fit the CTA's shared memory are merged by the
  *   last CTA of each (sequence, KV head), more by a merge kernel in the same
  *   stream. The CTA shape follows the sizes as for decode_attn_paged (one,
- *   two or three CTAs per SM), so results are reproducible per device.
+ *   two or four CTAs per SM), so results are reproducible per device.
  */
 int qk_norm_rope_append_int8(const pgqa_bf16 *q, const pgqa_bf16 *k, const pgqa_bf16 *v,
                              const pgqa_bf16 *gamma_q, const pgqa_bf16 *gamma_k,

@@ -10,6 +10,9 @@ accumulation adds about 1e-7. So there the ulp is counted as that of 2^-10
 (2^-17 absolute).
 """
 import numpy as np
+import torch
+
+import paged_gqa_decode_head_gb300 as pg
 
 BF16_ULP_FLOOR = 2.0 ** -17  # one bf16 ulp at 2^-10
 
@@ -45,3 +48,22 @@ def assert_bf16_close(gpu_bits, ref_bits, what="bf16"):
         r = widen(ref_bits)[tuple(idx)]
         raise AssertionError(f"{what}: {int((~ok).sum())} values beyond 1 ulp, first at {tuple(idx)}: "
                              f"gpu {g!r} vs oracle {r!r}")
+
+
+def walked(B, Hq, Hkv, P, max_pages, num_partitions):
+    """The library's rule for walking partitions (decode_walk_kernel): attention
+    alone over a grid of the two-CTA shape (one new token, g <= 6, more CTAs
+    than SMs, partitions of at most 2048 positions) whose states the merge
+    kernel merges (over 64 partitions, or more accumulators than its 96 KiB of
+    stages hold beside 5184 bytes of scratch), with few enough (sequence, KV
+    head) pairs that runs of partitions fill at least 7/8 of the SMs."""
+    np_used = pg.decode_attn_partition_count(B, Hkv, P, max_pages, num_partitions)
+    ppp = -(-max_pages // np_used)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = Hq // Hkv
+    pair = G <= 6 and np_used > 1 and ppp * P <= 2048 and B * Hkv * np_used > sms
+    merge_kernel = np_used > 64 or G * np_used * 128 * 4 + 5184 > 6 * 2 * 8192
+    heads = B * Hkv
+    per_head = sms // heads
+    return (pair and merge_kernel and heads <= sms and per_head * heads * 8 >= sms * 7
+            and -(-np_used // max(1, per_head)) >= 2)

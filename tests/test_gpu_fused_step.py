@@ -11,7 +11,7 @@ import oracle
 import paged_gqa_decode_head_gb300 as pg
 from paged_gqa_decode_head_gb300 import binding, inputs
 from paged_gqa_decode_head_gb300.runner import bf16_bits, to_device_bf16, to_device_i32
-from parity_util import assert_bf16_close
+from parity_util import assert_bf16_close, walked
 
 pytestmark = pytest.mark.gpu
 
@@ -128,25 +128,6 @@ def test_fused_step_matches_the_two_launches_bit_for_bit(num_partitions):
     for key in ("q_out", "kc", "vc", "ob"):
         assert np.array_equal(fused[key], two[key]), key
     assert np.array_equal(fused["of"], two["of"])
-
-
-def walked(B, Hq, Hkv, P, max_pages, num_partitions):
-    """The library's rule for walking partitions (decode_walk_kernel): attention
-    alone over a grid of the two-CTA shape (one new token, g <= 6, more CTAs
-    than SMs, partitions of at most 2048 positions) whose states the merge
-    kernel merges (over 64 partitions, or more accumulators than its 96 KiB of
-    stages hold beside 5184 bytes of scratch), with few enough (sequence, KV
-    head) pairs that runs of partitions fill at least 7/8 of the SMs."""
-    np_used = pg.decode_attn_partition_count(B, Hkv, P, max_pages, num_partitions)
-    ppp = -(-max_pages // np_used)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    G = Hq // Hkv
-    pair = G <= 6 and np_used > 1 and ppp * P <= 2048 and B * Hkv * np_used > sms
-    merge_kernel = np_used > 64 or G * np_used * 128 * 4 + 5184 > 6 * 2 * 8192
-    heads = B * Hkv
-    per_head = sms // heads
-    return (pair and merge_kernel and heads <= sms and per_head * heads * 8 >= sms * 7
-            and -(-np_used // max(1, per_head)) >= 2)
 
 
 @pytest.mark.parametrize("Hq,ctx,num_partitions", [

@@ -15,7 +15,7 @@ import torch
 import oracle
 import paged_gqa_decode_head_gb300 as pg
 from paged_gqa_decode_head_gb300 import inputs
-from parity_util import assert_bf16_close
+from parity_util import assert_bf16_close, walked
 from paged_gqa_decode_head_gb300.runner import DecodeStep, bf16_bits, to_device_bf16, to_device_i32
 
 pytestmark = pytest.mark.gpu
@@ -303,6 +303,26 @@ def test_decode_bad_page_and_context_are_masked_and_flagged():
     of, _ = gpu_decode(q[:1], kv2)
     assert pg.device_error_flags() & binding_flag("BAD_CONTEXT")
     assert np.all(of == 0)
+
+
+def test_walked_partitions_mask_and_flag_bad_pages_and_contexts():
+    """The same rules on a walked grid (runs of partitions per CTA): a refused
+    page is masked and flagged, a context longer than the table gives zeros
+    and a flag, the other sequences are unaffected."""
+    ctx = [3000, 2500, 1000]
+    kv = inputs.paged_kv(87, ctx, Hkv=8, page_size=16, fill_unused="normal")
+    q = inputs.query(87, len(ctx), 16)
+    assert walked(len(ctx), 16, 8, 16, kv.max_pages, 100)
+    kv.block_table[0, 40] = -3          # positions 640..655 of sequence 0 unreadable
+    kv.context_lens[2] = kv.max_pages * 16 + 1
+    of, _ = gpu_decode(q, kv, num_partitions=100)
+    flags = pg.device_error_flags()
+    assert flags & binding_flag("BAD_PAGE") and flags & binding_flag("BAD_CONTEXT")
+    assert np.isfinite(of).all()
+    assert np.all(of[2] == 0)
+    good = inputs.PagedKV(kv.k_cache, kv.v_cache, kv.block_table[1:2].copy(), kv.context_lens[1:2].copy(), 16)
+    ref = oracle.decode_attention(q[1:2], good.k_cache, good.v_cache, good.block_table, good.context_lens, SCALE)
+    assert np.abs(of[1:2] - ref).max() <= ATOL_F32
 
 
 def test_decode_workspace_too_small_is_refused():

@@ -1328,7 +1328,8 @@ cudaError_t launch_walk(const CUtensorMap &mk, const CUtensorMap &mv, const Spli
 // Partitions per CTA of the walked grid, or 0 when walking does not apply:
 // attention alone over a grid the two-CTA shape would run in several waves,
 // merged by merge_kernel, with few enough (sequence, KV head) pairs that
-// whole runs of partitions fill the SMs (at least 7/8 of them, one CTA each).
+// runs of partitions fill at least 7/8 of the walked shape's CTA slots (two
+// per SM for g <= 4, else one).
 int walk_partitions(bool pair, bool fused_merge, bool fused, int NCOL, int B, int Hkv, int num_partitions,
                     int sm_count)
 {

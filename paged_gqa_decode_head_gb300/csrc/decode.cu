@@ -924,14 +924,11 @@ template <int NCOL, int kS, int kCtas> struct WalkShape {
     static_assert(kSmem <= 232448, "at most 227 KB of shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
 };
-// Two CTAs per SM of 2 stages per warp where their records leave room
-// (NCOL <= 4), else one CTA of 3 stages.
-template <int NCOL>
-using WalkShapeFor = std::conditional_t<NCOL <= 4, WalkShape<NCOL, 2, 2>, WalkShape<NCOL, 3, 1>>;
-constexpr int walk_ctas_per_sm(int ncol)
-{
-    return ncol <= 4 ? WalkShapeFor<1>::kCtasPerSm : WalkShapeFor<6>::kCtasPerSm;
-}
+// Two CTAs per SM of 6 warps x 2 stages and their records (NCOL <= 4: for
+// g = 5, 6 the records leave no room for two, and one CTA per SM streams
+// less than the two-CTA shape, which those grids keep).
+constexpr int kWalkMaxCols = 4;
+template <int NCOL> using WalkShapeFor = WalkShape<NCOL, 2, 2>;
 
 template <int NCOL, typename S>
 __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
@@ -1327,16 +1324,16 @@ cudaError_t launch_walk(const CUtensorMap &mk, const CUtensorMap &mv, const Spli
 
 // Partitions per CTA of the walked grid, or 0 when walking does not apply:
 // attention alone over a grid the two-CTA shape would run in several waves,
-// merged by merge_kernel, with few enough (sequence, KV head) pairs that
-// runs of partitions fill at least 7/8 of the walked shape's CTA slots (two
-// per SM for g <= 4, else one).
+// merged by merge_kernel, with g <= 4 and few enough (sequence, KV head)
+// pairs that runs of partitions fill at least 7/8 of the walked shape's CTA
+// slots (two per SM).
 int walk_partitions(bool pair, bool fused_merge, bool fused, int NCOL, int B, int Hkv, int num_partitions,
                     int sm_count)
 {
-    if (!pair || fused_merge || fused)
+    if (!pair || fused_merge || fused || NCOL > kWalkMaxCols)
         return 0;
     const long heads = static_cast<long>(B) * Hkv;
-    const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * walk_ctas_per_sm(NCOL);
+    const long slots = static_cast<long>(sm_count > 0 ? sm_count : 1) * WalkShapeFor<1>::kCtasPerSm;
     if (heads > slots)
         return 0;
     const long per_head = slots / heads;
@@ -1520,13 +1517,11 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream)
     kp.walk = walk_partitions(pair, kp.fused_merge != 0, a.fused, NCOL, a.B, a.Hkv, a.num_partitions, a.sm_count);
     if (kp.walk) {
         grid.x = (a.num_partitions + kp.walk - 1) / kp.walk;
-        switch (NCOL) { // pair: NCOL <= the two-CTA shape's 6 warps
+        switch (NCOL) { // <= kWalkMaxCols
         case 1: err = launch_walk<1>(mk, mv, kp, grid, stream); break;
         case 2: err = launch_walk<2>(mk, mv, kp, grid, stream); break;
         case 3: err = launch_walk<3>(mk, mv, kp, grid, stream); break;
         case 4: err = launch_walk<4>(mk, mv, kp, grid, stream); break;
-        case 5: err = launch_walk<5>(mk, mv, kp, grid, stream); break;
-        case 6: err = launch_walk<6>(mk, mv, kp, grid, stream); break;
         default: return cudaErrorInvalidValue;
         }
     } else {

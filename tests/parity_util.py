@@ -53,10 +53,11 @@ def assert_bf16_close(gpu_bits, ref_bits, what="bf16"):
 def walked(B, Hq, Hkv, P, max_pages, num_partitions):
     """The library's rule for walking partitions (decode_walk_kernel): attention
     alone over a grid of the two-CTA shape (one new token, g <= 6, more CTAs
-    than SMs, partitions of at most 2048 positions) whose states the merge
-    kernel merges (over 64 partitions, or more accumulators than its 96 KiB of
-    stages hold beside 5184 bytes of scratch), with few enough (sequence, KV
-    head) pairs that runs of partitions fill at least 7/8 of the SMs."""
+    than SMs, partitions of at most 2048 positions) with g <= 4, whose states
+    the merge kernel merges (over 64 partitions, or more accumulators than its
+    96 KiB of stages hold beside 5184 bytes of scratch), and few enough
+    (sequence, KV head) pairs that runs of partitions fill at least 7/8 of the
+    CTA slots (two per SM)."""
     np_used = pg.decode_attn_partition_count(B, Hkv, P, max_pages, num_partitions)
     ppp = -(-max_pages // np_used)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -64,6 +65,7 @@ def walked(B, Hq, Hkv, P, max_pages, num_partitions):
     pair = G <= 6 and np_used > 1 and ppp * P <= 2048 and B * Hkv * np_used > sms
     merge_kernel = np_used > 64 or G * np_used * 128 * 4 + 5184 > 6 * 2 * 8192
     heads = B * Hkv
-    per_head = sms // heads
-    return (pair and merge_kernel and heads <= sms and per_head * heads * 8 >= sms * 7
+    slots = 2 * sms
+    per_head = slots // heads
+    return (pair and G <= 4 and merge_kernel and heads <= slots and per_head * heads * 8 >= slots * 7
             and -(-np_used // max(1, per_head)) >= 2)

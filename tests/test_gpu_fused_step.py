@@ -132,7 +132,7 @@ def test_fused_step_matches_the_two_launches_bit_for_bit(num_partitions):
 
 @pytest.mark.parametrize("Hq,ctx,num_partitions", [
     (8, [5000, 129, 1], 100),       # g = 1 (79 partitions); a one-partition sequence writes its output
-    (48, [3000, 40, 700], 40),      # g = 6: accumulators too large for the in-kernel merge
+    (24, [3000, 40, 700], 100),     # g = 3 (94 partitions of 32 positions)
     (32, [6000, 16, 2047], 200),    # one-page partitions: 4 of 6 warps own no chunk
     (16, [20000], 100),             # one sequence: 19 CTAs per KV head
 ])

@@ -907,8 +907,8 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
 // for bit; decode_step_paged keeps the two-CTA shape for such grids and still
 // matches the two launches.
 // Shared memory: the stages, their mbarriers and valid-row counts, the
-// warps' records of the current partition, the record fold's weights and an
-// abort flag.
+// warps' records of the current partition, the record fold's weights and a
+// flag that a copy never landed.
 template <int NCOL, int kS, int kCtas> struct WalkShape {
     static constexpr int kWarps = PairShape::kWarps;
     static constexpr int kStages = kS;
@@ -919,8 +919,8 @@ template <int NCOL, int kS, int kCtas> struct WalkShape {
     static constexpr int kRecFloats = (NCOL * kHeadDim + 2 * NCOL + 3) & ~3;
     static constexpr int kRecOffset = (kRowsOffset + kWarps * kStages * 4 + 15) & ~15;
     static constexpr int kWtsOffset = kRecOffset + kWarps * kRecFloats * 4;
-    static constexpr int kAbortOffset = kWtsOffset + (NCOL * kWarps + 2 * NCOL) * 4;
-    static constexpr int kSmem = 1024 /* alignment slack */ + kAbortOffset + 16;
+    static constexpr int kAbortedOffset = kWtsOffset + (NCOL * kWarps + 2 * NCOL) * 4;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kAbortedOffset + 16;
     static_assert(kSmem <= 232448, "at most 227 KB of shared memory per CTA");
     static_assert(kCtas * (kSmem + 1024) <= 233472, "228 KB of shared memory per SM, 1 KB reserved per CTA");
 };
@@ -949,7 +949,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBarOffset) + warp * kStages;
     int *stage_rows = reinterpret_cast<int *>(smem + S::kRowsOffset) + warp * kStages;
     float *recs = reinterpret_cast<float *>(smem + S::kRecOffset); // [kWarps][kRec]
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kAbortOffset);
+    volatile int *aborted = reinterpret_cast<volatile int *>(smem + S::kAbortedOffset);
     if (lane == 0) {
         if (warp == 0) {
             prefetch_tensormap(&tmap_k);
@@ -974,7 +974,7 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
     const int j0 = blockIdx.x * p.walk;
     const int j1 = min(n_parts, j0 + p.walk);
     if (threadIdx.x == 0)
-        *abort = 0;
+        *aborted = 0;
     __syncthreads();
     if (j0 >= j1) {
         grid_dependency_wait(); // keep the chain ordered even when idle
@@ -1112,19 +1112,19 @@ __global__ void __launch_bounds__(S::kThreads, S::kCtasPerSm)
             r += nc;
         }
         if (!ok && lane == 0)
-            *abort = 1;
+            *aborted = 1;
         // The partition's records, folded as the two-CTA shape folds them;
         // every warp's next chunks are in flight meanwhile.
         st.store_record(recs + warp * kRec);
         st.clear();
         __syncthreads();
-        if (*abort)
+        if (*aborted)
             break; // every thread sees the same flag after the barrier
         fold_records<NCOL, kWarps, false>(p, reinterpret_cast<const unsigned char *>(recs), kRec * 4,
                                           reinterpret_cast<float *>(smem + S::kWtsOffset), b, kvh, j, n_parts);
         __syncthreads();
     }
-    if (*abort) {
+    if (*aborted) {
         // A copy never landed: flag it and wait (bounded) for the copies
         // still in flight into this warp's stages.
         if (lane == 0)

@@ -130,19 +130,20 @@ def test_fused_step_matches_the_two_launches_bit_for_bit(num_partitions):
     assert np.array_equal(fused["of"], two["of"])
 
 
-@pytest.mark.parametrize("Hq,ctx,num_partitions", [
-    (8, [5000, 129, 1], 100),       # g = 1 (79 partitions); a one-partition sequence writes its output
-    (24, [3000, 40, 700], 100),     # g = 3 (94 partitions of 32 positions)
-    (32, [6000, 16, 2047], 200),    # one-page partitions: 4 of 6 warps own no chunk
-    (16, [20000], 100),             # one sequence: 19 CTAs per KV head
+@pytest.mark.parametrize("Hq,ctx,num_partitions,P", [
+    (8, [5000, 129, 1], 100, 16),   # g = 1 (79 partitions); a one-partition sequence writes its output
+    (24, [3000, 40, 700], 100, 16), # g = 3 (94 partitions of 32 positions)
+    (32, [6000, 16, 2047], 200, 16),  # one-page partitions: 4 of 6 warps own no chunk
+    (16, [20000], 100, 16),         # one sequence: 19 CTAs per KV head
+    (16, [20000, 333], 100, 64),    # 64-position pages: four chunks per page
 ])
-def test_walked_partitions_equal_the_two_cta_shape(Hq, ctx, num_partitions):
+def test_walked_partitions_equal_the_two_cta_shape(Hq, ctx, num_partitions, P):
     """Attention alone over these grids walks runs of partitions per CTA;
     the fused step keeps the two-CTA shape, one partition per CTA. Every
     partition is folded by the same warps in the same pairs and merged in
     the same order, so the two agree bit for bit, and both with the oracle."""
-    kv = inputs.paged_kv(370 + Hq + len(ctx), ctx, Hkv=8, page_size=16)
-    assert walked(len(ctx), Hq, 8, 16, kv.max_pages, num_partitions)
+    kv = inputs.paged_kv(370 + Hq + len(ctx) + P, ctx, Hkv=8, page_size=P)
+    assert walked(len(ctx), Hq, 8, P, kv.max_pages, num_partitions)
     tok = inputs.new_token(370 + Hq, len(ctx), Hq, 8)
     fused = check_fused(kv, tok, num_partitions)
     two = run_unfused(kv, tok, num_partitions)

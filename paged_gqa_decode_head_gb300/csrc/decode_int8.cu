@@ -14,8 +14,8 @@
 // GB300 design, as the bf16 kernel: one CTA per SM whose warps each own every
 // kW-th 16-position chunk of the partition and a private ring of stages (12
 // warps x 3 stages for short partitions, 16 warps x 3 for long ones, and
-// four or two CTAs per SM of 4 or 8 warps x 3 for grids of several waves
-// with short partitions: see Shape8); a chunk is two 2 KiB TMA tiles (K, V:
+// four or two CTAs per SM of 4 or 8 warps x 3 for grids of several waves:
+// see Shape8); a chunk is two 2 KiB TMA tiles (K, V:
 // 16 rows x 128 bytes, 128-byte swizzle) plus the chunk's 2 x 64 bytes of
 // scales, all completing on one mbarrier (one TMA load for both tiles and
 // one for both scale rows when the caller's buffers allow it). The fold runs fp16 tensor-core MMAs (m16n8k16) on codes
@@ -108,19 +108,21 @@ using Shape8Short = Shape8<12, 3, 1>;
 // 50.6, 12 x 4 one at a time 52.2, 8 x 6 in threes 58.3, 20 x 2 (spills)
 // 45.2.
 using Shape8Deep = Shape8<16, 3, 1, 1>;
-// Grids of several waves with short partitions run several CTAs per SM, so
-// that one CTA's start (table and context loads, first request) and end
-// (merge, state write) overlap the others' streaming: four of 4 warps x 3
-// stages (about 52 KiB each) for partitions up to 1024 positions, two of 8
-// warps x 3 stages (about 104 KiB) up to 2048; 16 warps per SM as above,
-// each folding one chunk at a time. B = 1, Hq = 32, T = 131072 (us, this
+// Grids of several waves run several CTAs per SM, so that one CTA's start
+// (table and context loads, first request) and end (merge, state write)
+// overlap the others' streaming: four of 4 warps x 3 stages (about 52 KiB
+// each) for partitions up to 1024 positions, two of 8 warps x 3 stages
+// (about 104 KiB) otherwise; 16 warps per SM as above, each folding one
+// chunk at a time. Two CTAs of 8 warps against one of 16 for longer
+// partitions (us): B = 64 ragged contexts, 4096-position partitions 364.1
+// against 398.4; B = 1, Hq = 32, T = 131072 with 2731-, 4096- and
+// 5462-position partitions 60.3 / 52.3 / 67.8 against 61.8 / 57.5 / 70.8. B = 1, Hq = 32, T = 131072 (us, this
 // shape / the earlier three of 4 x 4 or two of 6 x 4, in pairs): 512-position
 // partitions 58.9 / 64.9, 1024 52.5 / 60.3, 2048 56.3 / 60.0; three of
 // 4 x 4 one at a time 66.0 (512) and 62.5 (1024); 512-position partitions
 // on two of 8 x 3: 67.8.
 using Shape8Pair = Shape8<8, 3, 2, 1>;
 using Shape8Quad = Shape8<4, 3, 4, 1>;
-constexpr int kPairMaxPositions8 = 2048;
 constexpr int kQuadMaxPositions8 = 1024;
 
 struct Int8Params {
@@ -905,17 +907,18 @@ cudaError_t launch_decode_int8(const DecodeInt8Args &a, cudaStream_t stream)
         kp.eps = a.eps;
         kp.freqs = make_rope_freqs(a.rope_theta);
     }
-    // Grids of more than one wave (of one CTA per SM) with short partitions
-    // take four or two CTAs per SM (the fused step and attention alone
-    // alike, so they give equal bits); otherwise long partitions take 16
-    // warps x 3 stages, short ones 12 warps x 3 (both fold-bound).
+    // Grids of more than one wave (of one CTA per SM) take four (short
+    // partitions) or two CTAs per SM (the fused step and attention alone
+    // alike, so they give equal bits); one-wave grids take 16 warps x 3
+    // stages for long partitions, 12 warps x 3 for short ones (both
+    // fold-bound).
     const long part_positions = static_cast<long>(a.pages_per_part) * a.page_size;
     const bool waves = a.num_partitions > 1 &&
                        static_cast<long>(a.B) * a.Hkv * a.num_partitions > (a.sm_count > 0 ? a.sm_count : 1);
     Shape8Kind shape = part_positions >= kDeepChunks8 * kChunkTokens ? Shape8Kind::kDeep : Shape8Kind::kShort;
     if (waves && G <= Shape8Quad::kWarps && part_positions <= kQuadMaxPositions8)
         shape = Shape8Kind::kQuad;
-    else if (waves && G <= Shape8Pair::kWarps && part_positions <= kPairMaxPositions8)
+    else if (waves && G <= Shape8Pair::kWarps)
         shape = Shape8Kind::kPair;
     const bool in_kernel = shape == Shape8Kind::kQuad   ? merges_in_kernel<Shape8Quad>(G, a.num_partitions)
                            : shape == Shape8Kind::kPair ? merges_in_kernel<Shape8Pair>(G, a.num_partitions)

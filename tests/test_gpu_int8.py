@@ -260,13 +260,15 @@ def _fused_vs_two_launch(seed, ctx, Hq, num_partitions, page_size=16):
     ([2049, 40, 8000], 16, 70),
     ([700, 1], 64, 5),
     ([2049, 40, 3000], 64, 24),
+    ([12000, 11000, 9000, 12000, 5000, 12000, 7], 16, 3),
     ([512, 513], 8, 1),
 ])
 def test_int8_fused_step_equals_two_launches(ctx, Hq, num_partitions):
     """decode_step_paged_int8 writes the same codes and scales, the same
     rotated query and the same outputs (bit for bit) as the quantizing
     prologue followed by the INT8 attention (one and several CTAs per SM:
-    70 partitions of g = 2 run four per SM, 24 of g = 8 two per SM)."""
+    70 partitions of g = 2 run four per SM, 24 of g = 8 two per SM, and so
+    do 3 partitions of 4000 positions over 7 sequences)."""
     res, *_ = _fused_vs_two_launch(1300 + sum(ctx) % 97 + Hq, ctx, Hq, num_partitions)
     for name, a, b in zip(("k8", "v8", "k_scale", "v_scale", "q_out", "out_f32", "out_bf16"), res["fused"], res["two"]):
         assert np.array_equal(a, b, equal_nan=False), name
